@@ -1,0 +1,178 @@
+/*
+ * libnbx: paged KV-cache append and split-KV ("flash-decoding") decode attention
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * C ABI. Every buffer argument is a plain pointer to memory the caller owns; the
+ * library allocates and frees nothing and never synchronises the stream. Device
+ * pointers are marked [device], host values are passed by value. Streams are
+ * passed as `void*` holding a cudaStream_t (NULL = the legacy default stream).
+ *
+ * Layouts are row-major with the last dimension contiguous:
+ *   pool         [num_pages, h_kv, page_tokens, d]   one pool per K and per V
+ *   new_k/new_v  [n_tok, h_kv, d]
+ *   slot_mapping [n_tok]            int32, slot = page * page_tokens + position in page
+ *   q            [batch, rows, h_q, d]
+ *   block_table  [batch, max_pages] int32 page ids, -1 past each sequence
+ *   seq_lens     [batch]            int32 positions each sequence holds
+ *   out          [batch, rows, h_q, d] fp32
+ *
+ * Sources (pages the method is described on):
+ *   nbxtensor 0.0.1 wheel, nbxtensor/ops/attention_wrappers.py: paged_kv_append,
+ *     paged_decode_attention, decode_reduce (the boundary and its checks);
+ *   nbxtensor 0.0.1 wheel, nbxtensor/ops/paged_decode_attn.py: module docstring (pool
+ *     layout, slot mapping, block table), paged_kv_append_kernel, paged_decode_splits,
+ *     paged_decode_attn_split_kernel (the split partial);
+ *   TensorFold PR #1219: the rows-first grid (all rows of a split share its K/V from
+ *     L2), the fp8 cache, the merge's skip rule.
+ *
+ * Errors. Host-detectable problems return a negative nbx_status before anything is
+ * launched. Problems only the device can see (a slot or a page id outside the pool,
+ * a length outside its bounds, a wait that ran out of time) set bits in the optional
+ * [device] int32 status word with an atomic OR and skip the offending work; kernels
+ * never trap. The caller reads the word after synchronising; it is never cleared by
+ * the library.
+ */
+#ifndef NBX_H
+#define NBX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NBX_API __attribute__((visibility("default")))
+
+typedef enum {
+    NBX_F32 = 0,   /* IEEE binary32 */
+    NBX_BF16 = 1,  /* bfloat16 */
+    NBX_E4M3 = 2   /* OCP FP8 E4M3 (FN: no infinities, max 448), with one fp32 scale per pool */
+} nbx_dtype;
+
+typedef enum {
+    NBX_OK = 0,
+    NBX_ERR_NULL = -1,        /* a required pointer is NULL */
+    NBX_ERR_SHAPE = -2,       /* sizes that do not fit together, or outside the supported set */
+    NBX_ERR_DTYPE = -3,       /* a dtype code this call does not take */
+    NBX_ERR_PAGE_ALIGN = -4,  /* page_tokens is not a multiple of NBX_TILE_POSITIONS */
+    NBX_ERR_WORKSPACE = -5,   /* workspace smaller than nbx_paged_decode_workspace_bytes() */
+    NBX_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
+    NBX_ERR_ALIGN = -7,       /* a buffer is not 16-byte aligned */
+    NBX_ERR_VALUE = -8        /* a scalar argument is not finite or a scale is not positive */
+} nbx_status;
+
+/* Bits of the device status word. */
+#define NBX_DEV_BAD_SLOT 0x1   /* an append slot outside [0, num_pages * page_tokens): token skipped */
+#define NBX_DEV_BAD_PAGE 0x2   /* a block-table entry inside a sequence is -1 or >= num_pages: tile skipped */
+#define NBX_DEV_BAD_LEN 0x4    /* seq_lens[b] < 0, > max_seq_len or > max_pages * page_tokens: sequence read as empty */
+#define NBX_DEV_TIMEOUT 0x8    /* a bounded wait inside a kernel gave up: the output is incomplete */
+
+/* Positions per staged tile: every page must hold a whole number of tiles, so no
+ * tile straddles two pages (paged_decode_attention's "ZERO FALLBACK" check). */
+#define NBX_TILE_POSITIONS 16
+/* The split rule (nbxtensor/ops/paged_decode_attn.py, paged_decode_splits). */
+#define NBX_SPLIT_POSITIONS 256
+#define NBX_MAX_SPLITS 64
+
+/*
+ * nbx_paged_kv_append -- write new positions into the pools through the slot mapping.
+ * (nbxtensor/ops/attention_wrappers.py, paged_kv_append; nbxtensor/ops/paged_decode_attn.py,
+ * paged_kv_append_kernel.)
+ *
+ * For token t and KV head h: page = slot_mapping[t] / page_tokens, pos = slot_mapping[t] %
+ * page_tokens, k_pool[page, h, pos, :] = cast(new_k[t, h, :] * (1 / k_scale)), the same for V.
+ * The reciprocal is taken once in fp32 on the host; the cast rounds to nearest even (bf16,
+ * E4M3 with saturation to +-448) or copies (fp32).
+ *
+ *   new_k, new_v  [device] [n_tok, h_kv, d] in new_dtype (NBX_F32 or NBX_BF16)
+ *   n_tok         tokens to write; 0 returns NBX_OK without a launch
+ *   k_pool, v_pool [device] [num_pages, h_kv, page_tokens, d] in pool_dtype (any nbx_dtype)
+ *   slot_mapping  [device] int32 [n_tok]; entries must be distinct. A slot outside
+ *                 [0, num_pages*page_tokens) sets NBX_DEV_BAD_SLOT and the token is skipped.
+ *   k_scale, v_scale  dequantisation scales of the pools (finite, > 0; use 1 unless E4M3)
+ *   status        [device] int32 or NULL
+ *   stream        cudaStream_t
+ * Requirements: d a multiple of 16 and <= 1024; all buffers 16-byte aligned.
+ */
+NBX_API int nbx_paged_kv_append(const void* new_k, const void* new_v, int new_dtype, int n_tok, int h_kv, int d,
+                                void* k_pool, void* v_pool, int pool_dtype, int num_pages, int page_tokens,
+                                const int32_t* slot_mapping, float k_scale, float v_scale, int32_t* status,
+                                void* stream);
+
+/*
+ * nbx_paged_decode_workspace_bytes -- bytes of workspace nbx_paged_decode_attn needs for
+ * these sizes (the split plan, the work list, the merge tickets and the fp32 split partials).
+ * Returns 0 if the sizes are invalid. max_seq_len is the host-known bound on seq_lens.
+ */
+NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len);
+
+/*
+ * nbx_paged_decode_attn -- split-KV decode attention read through the block table.
+ * (nbxtensor/ops/attention_wrappers.py, paged_decode_attention; nbxtensor/ops/paged_decode_attn.py,
+ * paged_decode_splits and paged_decode_attn_split_kernel; TensorFold PR #1219, rows-first grid.)
+ *
+ * For sequence b, query row r and query head h: the row sits at position
+ * p = seq_lens[b] - rows + r and attends keys 0..p of KV head h / (h_q / h_kv):
+ *   s_j = scale * k_scale * (q . k_j),  out = v_scale * sum_j e^(s_j - max s) v_j / sum_j e^(s_j - max s).
+ * A row with no visible key (p < 0, or seq_lens[b] == 0) gets 0. Each sequence is cut into
+ * min(ceil(len/256), 64) splits of whole pages; each split's unnormalised partial (m, l, acc)
+ * is computed with an fp32 online softmax and the partials are merged in ascending split order
+ * (a split with m = -inf is skipped, so NaN inputs reach the output). The result does not
+ * depend on the physical page ids or on the order the work runs in.
+ *
+ *   q            [device] [batch, rows, h_q, d], q_dtype NBX_F32 or NBX_BF16
+ *   k_pool, v_pool [device] [num_pages, h_kv, page_tokens, d] in pool_dtype
+ *   block_table  [device] int32 [batch, max_pages]
+ *   seq_lens     [device] int32 [batch]
+ *   max_seq_len  host bound on seq_lens (sizes the splits and the workspace);
+ *                must be <= max_pages * page_tokens
+ *   scale        softmax scale (finite); k_scale, v_scale: pool scales (finite, > 0)
+ *   out          [device] fp32 [batch, rows, h_q, d]
+ *   workspace    [device] at least nbx_paged_decode_workspace_bytes(...) bytes, 256-byte aligned;
+ *                its contents need no initialisation and are overwritten
+ *   status       [device] int32 or NULL
+ *   stream       cudaStream_t
+ * Requirements: h_q % h_kv == 0; d in {64, 128, 256}; page_tokens a multiple of
+ * NBX_TILE_POSITIONS; q, pools and out 16-byte aligned. batch == 0 returns NBX_OK without a launch.
+ * Calls on one workspace must not overlap on the GPU.
+ */
+NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
+                                  const void* k_pool, const void* v_pool, int pool_dtype, int num_pages, int h_kv,
+                                  int page_tokens, const int32_t* block_table, int max_pages,
+                                  const int32_t* seq_lens, int max_seq_len, float scale, float k_scale,
+                                  float v_scale, float* out, void* workspace, size_t workspace_bytes,
+                                  int32_t* status, void* stream);
+
+/*
+ * nbx_paged_decode_merge -- the fixed-order merge of split partials on its own.
+ * (nbxtensor/ops/attention_wrappers.py, decode_reduce; TensorFold PR #1219, the merge's skip rule.)
+ *
+ * For each row i: M = max_s m[i,s], L = sum_s l[i,s] e^(m[i,s]-M),
+ * out[i,:] = sum_s acc[i,s,:] e^(m[i,s]-M) / L, s ascending, skipping splits with m = -inf.
+ * A row with no live split gets 0. m is in natural-log units (the running max of the scores).
+ *
+ *   acc_part [device] fp32 [n_rows, splits, d];  m_part, l_part [device] fp32 [n_rows, splits]
+ *   out      [device] fp32 [n_rows, d]
+ * Requirements: 1 <= splits <= 4096, 1 <= d <= 1024. n_rows == 0 returns NBX_OK without a launch.
+ */
+NBX_API int nbx_paged_decode_merge(const float* acc_part, const float* m_part, const float* l_part, int n_rows,
+                                   int splits, int d, float* out, void* stream);
+
+/*
+ * nbx_set_decode_grid_limit -- cap the number of CTAs nbx_paged_decode_attn launches (0 = the
+ * default, two per SM). Process-wide; the output is bit-identical for every value.
+ */
+NBX_API void nbx_set_decode_grid_limit(int max_ctas);
+
+/* A static, human-readable name for an nbx_status value. */
+NBX_API const char* nbx_status_string(int status);
+
+/* ABI version of this header (major * 100 + minor). */
+NBX_API int nbx_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NBX_H */

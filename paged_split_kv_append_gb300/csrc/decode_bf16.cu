@@ -1,0 +1,6 @@
+// Instantiations of the split-KV partial kernel for BF16 pools (query fp32 / bf16, head dim 64 / 128 / 256).
+#include "decode_kernels.cuh"
+
+namespace nbx {
+NBX_DECODE_FOR_POOL(BF16)
+}  // namespace nbx

@@ -1,0 +1,109 @@
+// Host-side internals of libnbx: launch parameter blocks, the workspace layout and the
+// per-device launch facts. Not part of the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/nbx.h"
+
+namespace nbx {
+
+constexpr float kLog2eHost = 1.4426950408889634f;
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int max_smem_optin;
+};
+
+// Facts of the current device, queried once per device.
+const DeviceInfo& device_info();
+
+struct AppendParams {
+  const void* new_k;
+  const void* new_v;
+  void* k_pool;
+  void* v_pool;
+  const int32_t* slot_mapping;
+  int32_t* status;
+  int n_tok, h_kv, d, num_pages, page_tokens;
+  float k_inv, v_inv;
+};
+
+cudaError_t append_dispatch(const AppendParams& p, int new_dtype, int pool_dtype, cudaStream_t stream);
+
+// ---------------------------------------------------------------- decode
+constexpr int kTileN = NBX_TILE_POSITIONS;  // positions per staged tile
+constexpr int kQB = 4;                      // query vectors (rows x heads of one KV head) per work unit
+constexpr int kConsumerWarps = 4;
+constexpr int kDecodeThreads = (kConsumerWarps + 1) * 32;
+
+// One sequence of the split plan.
+struct SeqPlan {
+  int32_t len;       // positions read (0 if the length was out of bounds)
+  int32_t seg;       // positions per split (a whole number of pages)
+  int32_t n_splits;  // non-empty splits: ceil(len / seg)
+  int32_t pad;
+};
+
+// One (sequence, split) of the work list; a work unit is (entry, KV head, row block).
+struct Entry {
+  int32_t b, s, start, end;
+};
+
+// Byte offsets of the workspace sections (each 256-byte aligned).
+struct WorkspaceLayout {
+  size_t header;    // int32[64]: [0] entries in the list, [1] work counter
+  size_t plan;      // SeqPlan[batch]
+  size_t entries;   // Entry[batch * max_splits]
+  size_t tickets;   // int32[batch * h_kv * row_blocks]
+  size_t m_part;    // f32[batch * rows * h_q * max_splits]   (log2 units)
+  size_t l_part;    // f32[batch * rows * h_q * max_splits]
+  size_t acc_part;  // f32[batch * rows * h_q * max_splits * d]
+  size_t total;
+  int max_splits;
+  int row_blocks;
+};
+
+// Returns false if the sizes overflow.
+bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* out);
+
+int splits_for(int length);
+
+struct DecodeParams {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  float* out;
+  int32_t* status;
+  // workspace sections
+  int32_t* header;
+  SeqPlan* plan;
+  Entry* entries;
+  int32_t* tickets;
+  float* m_part;
+  float* l_part;
+  float* acc_part;
+  int batch, rows, h_q, h_kv, group, d, num_pages, page_tokens, max_pages, max_seq_len;
+  int max_splits, row_blocks;
+  float qk_scale_log2;  // scale * k_scale * log2(e): scores in log2 units
+  float v_scale;
+};
+
+cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);
+
+struct MergeParams {
+  const float* acc_part;
+  const float* m_part;
+  const float* l_part;
+  float* out;
+  int n_rows, splits, d;
+};
+
+cudaError_t merge_dispatch(const MergeParams& p, cudaStream_t stream);
+
+}  // namespace nbx

@@ -1,0 +1,127 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol of
+include/nbx.h, and refuses bad arguments on the host before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_split_kv_append_gb300 as nbx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nbx.h")
+
+NULL = None
+FAKE = ctypes.c_void_p(0x10000)          # a 16-byte aligned address that is never dereferenced
+FAKE_ODD = ctypes.c_void_p(0x10008)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nbx.build()
+    return nbx.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"NBX_API\s+[\w\s\*]+?\b(nbx_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("nbx_paged_kv_append", "nbx_paged_decode_workspace_bytes", "nbx_paged_decode_attn",
+              "nbx_paged_decode_merge", "nbx_status_string", "nbx_abi_version", "nbx_set_decode_grid_limit"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+
+
+def test_status_strings(lib):
+    assert nbx.nbx_status_string(0) == "ok"
+    for code in range(-1, -9, -1):
+        assert nbx.nbx_status_string(code) != "unknown status"
+    assert lib.nbx_abi_version() == 100
+
+
+def _append(lib, **kw):
+    a = dict(new_k=FAKE, new_v=FAKE, new_dtype=0, n_tok=4, h_kv=2, d=64, k_pool=FAKE, v_pool=FAKE, pool_dtype=1,
+             num_pages=8, page_tokens=16, slots=FAKE, k_scale=1.0, v_scale=1.0, status=NULL, stream=NULL)
+    a.update(kw)
+    return lib.nbx_paged_kv_append(a["new_k"], a["new_v"], a["new_dtype"], a["n_tok"], a["h_kv"], a["d"],
+                                   a["k_pool"], a["v_pool"], a["pool_dtype"], a["num_pages"], a["page_tokens"],
+                                   a["slots"], a["k_scale"], a["v_scale"], a["status"], a["stream"])
+
+
+def test_append_host_checks(lib):
+    assert _append(lib, n_tok=0) == 0                        # nothing to write: no launch
+    assert _append(lib, new_k=NULL) == -1
+    assert _append(lib, slots=NULL) == -1
+    assert _append(lib, d=72) == -2
+    assert _append(lib, h_kv=0) == -2
+    assert _append(lib, n_tok=-1) == -2
+    assert _append(lib, new_dtype=2) == -3                   # e4m3 input is not taken
+    assert _append(lib, pool_dtype=7) == -3
+    assert _append(lib, k_pool=FAKE_ODD) == -7
+    assert _append(lib, v_scale=0.0) == -8
+    assert _append(lib, k_scale=float("nan")) == -8
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, q_dtype=1, batch=2, rows=1, h_q=8, d=128, k_pool=FAKE, v_pool=FAKE, pool_dtype=1,
+             num_pages=100, h_kv=2, page_tokens=16, bt=FAKE, max_pages=10, lens=FAKE, max_seq_len=160,
+             scale=0.1, k_scale=1.0, v_scale=1.0, out=FAKE, ws=FAKE, ws_bytes=1 << 30, status=NULL, stream=NULL)
+    a.update(kw)
+    return lib.nbx_paged_decode_attn(a["q"], a["q_dtype"], a["batch"], a["rows"], a["h_q"], a["d"], a["k_pool"],
+                                     a["v_pool"], a["pool_dtype"], a["num_pages"], a["h_kv"], a["page_tokens"],
+                                     a["bt"], a["max_pages"], a["lens"], a["max_seq_len"], a["scale"],
+                                     a["k_scale"], a["v_scale"], a["out"], a["ws"], a["ws_bytes"], a["status"],
+                                     a["stream"])
+
+
+def test_decode_host_checks(lib):
+    assert _decode(lib, batch=0) == 0                        # empty batch: no launch
+    assert _decode(lib, h_q=6, h_kv=4) == -2                 # h_q % h_kv
+    assert _decode(lib, d=96) == -2
+    assert _decode(lib, rows=0) == -2
+    assert _decode(lib, max_seq_len=161) == -2               # more positions than the table holds
+    assert _decode(lib, page_tokens=24, max_seq_len=100) == -4   # a tile would straddle two pages
+    assert _decode(lib, q_dtype=2) == -3
+    assert _decode(lib, pool_dtype=5) == -3
+    assert _decode(lib, scale=float("inf")) == -8
+    assert _decode(lib, v_scale=-1.0) == -8
+    assert _decode(lib, bt=NULL) == -1
+    assert _decode(lib, ws=NULL) == -1
+    assert _decode(lib, out=FAKE_ODD) == -7
+    assert _decode(lib, ws=ctypes.c_void_p(0x10010)) == -7   # workspace must be 256-byte aligned
+    need = lib.nbx_paged_decode_workspace_bytes(2, 1, 8, 2, 128, 160)
+    assert _decode(lib, ws_bytes=need - 1) == -5
+
+
+def test_workspace_bytes(lib):
+    f = lib.nbx_paged_decode_workspace_bytes
+    assert f(2, 1, 8, 3, 128, 100) == 0                      # invalid sizes -> 0
+    small = f(32, 1, 32, 8, 128, 8192)
+    big = f(32, 1, 32, 8, 128, 131072)
+    assert 0 < small < big
+    # the fp32 partials dominate: batch * rows * h_q * splits(max_seq_len) * (d + 2) floats
+    assert big >= 32 * 32 * 64 * 130 * 4
+    assert small >= 32 * 32 * 32 * 130 * 4
+
+
+def test_merge_host_checks(lib):
+    f = lib.nbx_paged_decode_merge
+    assert f(FAKE, FAKE, FAKE, 0, 4, 64, FAKE, NULL) == 0
+    assert f(FAKE, FAKE, FAKE, 3, 0, 64, FAKE, NULL) == -2
+    assert f(FAKE, FAKE, FAKE, 3, 4, 0, FAKE, NULL) == -2
+    assert f(NULL, FAKE, FAKE, 3, 4, 64, FAKE, NULL) == -1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(nbx, "_lib", None)
+    monkeypatch.setattr(nbx._build, "LIB", str(tmp_path / "missing" / "libnbx.so"))
+    with pytest.raises(nbx.NbxLibraryMissing):
+        nbx.lib()
