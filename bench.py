@@ -333,17 +333,25 @@ def all_reduce_sum(x: float, world: int) -> float:
     return float(t.item())
 
 
-def config_block(case, args):
+def config_block(case, args, arm: str = "gpu"):
     cfg = case.cfg
-    lens = {"fixed": f"fixed {list(cfg.lens[1])[:4]}{'...' if len(cfg.lens[1]) > 4 else ''}",
-            "uniform": f"uniform[{cfg.lens[1]},{cfg.lens[2]}]",
-            "loguniform": f"log-uniform[{cfg.lens[1]},{cfg.lens[2]}]"}[cfg.lens[0]]
+    kind = cfg.lens[0]
+    if kind == "fixed":
+        vals = list(cfg.lens[1])
+        lens = f"fixed {vals[:4]}{'...' if len(vals) > 4 else ''}"
+    elif kind == "uniform":
+        lens = f"uniform[{cfg.lens[1]},{cfg.lens[2]}]"
+    else:
+        lens = f"log-uniform[{cfg.lens[1]},{cfg.lens[2]}]"
     return {"workload": cfg.name, "batch": cfg.batch, "rows": cfg.rows, "h_q": cfg.h_q, "h_kv": cfg.h_kv,
             "d": cfg.d, "page_tokens": cfg.page_tokens, "kv_dtype": cfg.pool_dtype, "q_dtype": cfg.q_dtype,
             "seq_lens": f"{lens} seed {cfg.seed}", "kv_bytes_per_step": int(case.kv_bytes()),
-            "l2": "flushed before every timed step (write of 2x L2, outside the events)",
-            "step": "append of the step's new positions + split plan + split-KV partial with fused merge",
-            "timing": "CUDA events per step around a CUDA-graph replay of the step"}
+            "l2": "flushed before every timed step (write of 2x L2, outside the events)" if arm == "gpu"
+            else "n/a (CPU)",
+            "step": "append of the step's new positions + split plan + split-KV partial with fused merge"
+            if arm == "gpu" else "the oracle's append of the new positions + float64 attention, bounded sample",
+            "timing": "CUDA events per step around a CUDA-graph replay of the step" if arm == "gpu"
+            else "wall clock (time.perf_counter) around each sample"}
 
 
 def main():
@@ -451,7 +459,7 @@ def run_reference(args):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded: workloads/)",
-        "config": config_block(leg.case, args),
+        "config": config_block(leg.case, args, arm="oracle"),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"per step ~{per_step:.3f} s: " + leg.describe(tot_groups // max(1, args.steps))},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -146,7 +146,6 @@ NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int row
   p.header = reinterpret_cast<int32_t*>(ws + w.header);
   p.plan = reinterpret_cast<SeqPlan*>(ws + w.plan);
   p.entries = reinterpret_cast<Entry*>(ws + w.entries);
-  p.tickets = reinterpret_cast<int32_t*>(ws + w.tickets);
   p.m_part = reinterpret_cast<float*>(ws + w.m_part);
   p.l_part = reinterpret_cast<float*>(ws + w.l_part);
   p.acc_part = reinterpret_cast<float*>(ws + w.acc_part);

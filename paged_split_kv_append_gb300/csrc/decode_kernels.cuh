@@ -1,43 +1,38 @@
-// Kernels 2 and 3: the split plan, the per-(split, KV head, row block) partial and the
-// fixed-order merge of split-KV decode attention read through a block table.
+// Kernels 2 and 3: the per-(split, KV head, row block) partial and the fixed-order merge of
+// split-KV decode attention read through a block table.
 //
 // Method (nbxtensor/ops/paged_decode_attn.py, paged_decode_splits and
 // paged_decode_attn_split_kernel; nbxtensor/ops/attention_wrappers.py, decode_reduce):
-// every sequence is cut into min(ceil(len/256), 64) splits of whole pages; each split
-// runs an online softmax over its keys and stores an unnormalised partial (m, l, acc);
-// the partials of a query row are merged in ascending split order.
+// every sequence is cut into min(ceil(len/256), 64) splits of whole pages; each split runs an
+// online softmax over its keys and stores an unnormalised partial (m, l, acc); the partials of
+// a query row are merged in ascending split order.
 //
-// GB300 design:
-//  * plan_kernel (one CTA) reads the device lengths, computes every sequence's split
-//    plan and writes a work list of (sequence, split) entries ordered longest split
-//    first, so the persistent partial kernel balances a ragged batch.
-//  * decode_partial_kernel is persistent: 2 CTAs per SM pull work units
-//    u = (entry, KV head, row block) from an atomic counter. Row blocks are the fastest
-//    index, so all query rows of one split run side by side and share its K/V from L2
-//    (TensorFold PR #1219, the rows-first grid). A unit covers kQB = 4 query vectors
-//    (rows x GQA heads of one KV head), so each K/V tile is read once for the whole
-//    GQA group instead of once per query head.
-//  * One producer warp streams page tiles (16 positions of one KV head, one contiguous
-//    block of the pool) into a ring of shared-memory stages with cp.async.bulk and
-//    mbarrier transaction counts, running ahead across unit boundaries; it also stages
-//    each unit's query vectors. A tile never straddles a page: split starts are page
-//    aligned and 16 divides the page.
-//  * Four consumer warps compute. Scores: 8 (or 4, 16) lanes share one position, each
-//    holding 16 elements of the 4 query vectors in registers; packed fp32 FMAs
-//    (fma.rn.f32x2) form partial dots and a transposing shuffle reduction leaves each
-//    lane with one (position, vector) score. The online softmax works in log2 units and
-//    rescales lazily: the running max moves only when a score exceeds it by more than
-//    kTau (the accumulated weights stay below 2^kTau times the tile count, exact in
-//    fp32), so the rescale branch is almost never taken. P*V: every lane owns D/32
-//    output elements of all 4 vectors and accumulates all positions of its warp.
-//  * Epilogue: the four warps' states are merged in fixed warp order through shared
-//    memory. A one-split sequence writes the normalised output directly; otherwise the
-//    unit stores its partial, and the CTA that takes the last ticket of its
-//    (sequence, KV head, row block) merges all splits in ascending order. No inter-CTA
-//    waits, no atomics on values: the output is bit-identical under any schedule and
-//    any physical page placement.
-//  * Every wait is bounded; on timeout the kernel records NBX_DEV_TIMEOUT, drains its
-//    copies in flight and returns.
+// GB300 design of decode_partial_kernel:
+//  * Persistent: kMinBlocks CTAs per SM pull work units u = (entry, KV head, row block) from
+//    an atomic counter, in the plan kernel's order (longest split first). Row blocks are the
+//    fastest index, so all query rows of one split run side by side and share its K/V from L2
+//    (TensorFold PR #1219, the rows-first grid). A unit covers kQB = 4 query vectors (rows x
+//    GQA heads of one KV head): each K/V tile is read once for the whole GQA group.
+//  * One producer warp streams 16-position page tiles of one KV head (one contiguous block of
+//    the pool each, two per stage) into a ring of shared-memory stages with cp.async.bulk,
+//    completing on mbarrier transaction counts, and stages every unit's query vectors and
+//    metadata. It runs ahead across unit boundaries. A tile never straddles a page: split
+//    starts are page aligned and 16 divides the page.
+//  * Every consumer warp takes a fixed quarter of every stage (so every partial sum has a
+//    fixed order, and the stages are consumed in ring order by all warps). Scores: LPT lanes share one position and each
+//    holds 16 elements of the 4 query vectors as packed fp32 pairs (fma.rn.f32x2); a lane group
+//    scores TPG positions per pass and a transposing shuffle reduction leaves each lane with one
+//    (position, vector) score. Online softmax in log2 units with a lazy rescale: the running max
+//    moves only when a pass's max exceeds it by more than kTau, so the rescale branch is rare
+//    and the weights stay below 2^kTau (exact enough in fp32). P*V: each lane owns D/32 output
+//    elements of the 4 vectors.
+//  * Epilogue: the four warps' states are merged in fixed warp order through double-buffered
+//    shared memory behind one bounded barrier. A one-split sequence writes its normalised
+//    output; otherwise the unit stores its partial and decode_merge_kernel (launched after it)
+//    merges the splits in ascending order. No atomics on values and fixed reduction orders:
+//    the output is bit-identical under any schedule and any physical page placement.
+//  * Every wait is bounded; on timeout the kernel records NBX_DEV_TIMEOUT, lets its copies in
+//    flight land and returns.
 #pragma once
 
 #include "nbx_device.cuh"
@@ -46,95 +41,89 @@
 namespace nbx {
 
 constexpr float kTau = 8.0f;                 // lazy-rescale threshold, log2 units
-constexpr int kSmemPerCta = 112 * 1024;      // two CTAs per SM
+constexpr int kSmemPerSm = 228 * 1024;       // shared memory of one SM (1 KB of it reserved per CTA)
 
 struct UnitMeta {
-  int32_t b, s, h, rb, start, end, n_splits, len;
+  int32_t b, s, h, start, end, n_splits, nvec, pad;
+  int32_t pos[kQB];    // last key each vector sees (causal row position); -1 for a missing vector
+  int64_t orow[kQB];   // output row (b * rows + r) * h_q + h * group + g
 };
 
 template <class PT, class QT, int D>
 struct DecodeCfg {
-  static constexpr int kLPT = D / 16;                 // lanes per position in the score layout
-  static constexpr int kTG = 32 / kLPT;               // positions per warp pass
-  static constexpr int kNV = 16 / PT::kEPV;           // 16-byte K vectors per lane
-  static constexpr int kVPL = D / 32;                 // output elements per lane in the P*V layout
-  static constexpr int kGroups = kTileN / kTG;        // warp passes per tile
-  static constexpr int kTileBytes = kTileN * D * PT::kBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kLPT = D / 16;                  // lanes per position in the score layout
+  static constexpr int kTPG = kLPT >= 8 ? 2 : 1;       // positions each lane group scores per pass
+  static constexpr int kTG = 32 / kLPT;                // lane groups per warp
+  static constexpr int kPassTok = kTG * kTPG;          // positions per warp pass
+  static constexpr int kStageTok = 2 * kTileN;         // positions per stage: two 16-position page tiles
+  static constexpr int kWarpTok = kStageTok / kConsumerWarps;   // positions of a stage each warp takes
+  static constexpr int kWarpPasses = kWarpTok / kPassTok;
+  static constexpr int kNV = 16 / PT::kEPV;            // 16-byte K vectors per lane
+  static constexpr int kVPL = D / 32;                  // output elements per lane in the P*V layout
+  static constexpr int kTileBytes = kTileN * D * PT::kBytes;     // one 16-position tile of K (or V)
+  static constexpr int kHalfBytes = kStageTok * D * PT::kBytes;  // the K (or V) part of a stage
+  static constexpr int kStageBytes = 2 * kHalfBytes;
   static constexpr int kQBytes = kQB * D * QT::kBytes;
-  // shared memory carve-up (bytes, each section 128-byte aligned)
-  static constexpr int kRedAccBytes = kConsumerWarps * kQB * D * 4;
-  static constexpr int kRedMLBytes = kConsumerWarps * kQB * 4 * 2;
-  static constexpr int kPBufBytes = kConsumerWarps * kTG * kQB * 4;
-  static constexpr int kMergeBytes = kQB * NBX_MAX_SPLITS * 4 * 2 + kQB * 4 * 4;
-  static constexpr int kFixed = ((2 * kQBytes + 127) / 128) * 128 + kRedAccBytes + 128 + kPBufBytes + 128 +
-                                kMergeBytes + 128 + 2 * (int)sizeof(UnitMeta) + 1024;
+  static constexpr int kRedFloats = kConsumerWarps * (kQB * D + 2 * kQB);   // one slot
+  static constexpr int kPBufBytes = kConsumerWarps * kPassTok * kQB * 8;      // (p, p) pairs
+  static constexpr int kFixed = 2 * kQBytes + 2 * kRedFloats * 4 + kPBufBytes + 2 * (int)sizeof(UnitMeta) + 2048;
+  // resident CTAs per SM: 3 (2 at head dim 256, where the registers allow no more), fewer when
+  // shared memory cannot hold two stages for each of them
+  static constexpr int kBlocksBySmem = kSmemPerSm / (kFixed + 2 * kStageBytes + 1024);
+  static constexpr int kMinBlocks = (D <= 128 ? 3 : 2) < kBlocksBySmem ? (D <= 128 ? 3 : 2)
+                                                                        : (kBlocksBySmem < 1 ? 1 : kBlocksBySmem);
+  static constexpr int kSmemPerCta = kSmemPerSm / kMinBlocks - 1024;
   static constexpr int kStagesRaw = (kSmemPerCta - kFixed) / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 16 ? 16 : (kStagesRaw < 2 ? 2 : kStagesRaw);
-  static_assert(kTileN % kTG == 0, "a tile holds whole warp passes");
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
+  static_assert(kWarpTok % kPassTok == 0, "a warp's share of a stage holds whole passes");
   static_assert(kLPT >= 4 && kLPT <= 16, "head dim 64..256");
 };
 
 struct SmemLayout {
   char* stages;
   char* qbuf;        // [2][kQBytes]
-  float* red_acc;    // [warps][kQB][D]
-  float* red_m;      // [warps][kQB]
-  float* red_l;      // [warps][kQB]
-  float* pbuf;       // [warps][kTG][kQB]
-  float* mg_m;       // [kQB][max splits]
-  float* mg_w;       // [kQB][max splits]
-  float* mg_scale;   // [kQB]
-  int* mg_dead;      // [kQB]
+  float* red;        // [2][warps][kQB*D acc | kQB m | kQB l]
+  f32x2* pbuf;       // [warps][kPassTok][kQB] (p, p) pairs
   UnitMeta* meta;    // [2]
-  int* stage_ok;     // [stages]
-  int* flags;        // [0] abort, [1] last-ticket, [2] tiles issued
+  int* stage_ok;     // [stages] bit h: tile h of the stage was copied
+  int* flags;        // [0] abort, [2] tiles issued
   uint64_t* full;    // [stages]
   uint64_t* empty;   // [stages]
   uint64_t* qfull;   // [2]
   uint64_t* qempty;  // [2]
-  uint64_t* cbar;    // consumer-warp barrier (count: consumer threads)
+  uint64_t* cbar;    // consumer-warp barrier
 };
 
-template <class C, int D>
-__device__ __forceinline__ SmemLayout carve(char* base) {
-  SmemLayout s;
-  char* p = base;
-  auto take = [&](int bytes) {
-    char* r = p;
-    p += ((bytes + 127) / 128) * 128;
-    return r;
-  };
-  s.stages = take(C::kStages * C::kStageBytes);
-  s.qbuf = take(2 * C::kQBytes);
-  s.red_acc = reinterpret_cast<float*>(take(C::kRedAccBytes));
-  s.red_m = reinterpret_cast<float*>(take(kConsumerWarps * kQB * 4));
-  s.red_l = reinterpret_cast<float*>(take(kConsumerWarps * kQB * 4));
-  s.pbuf = reinterpret_cast<float*>(take(C::kPBufBytes));
-  s.mg_m = reinterpret_cast<float*>(take(kQB * NBX_MAX_SPLITS * 4));
-  s.mg_w = reinterpret_cast<float*>(take(kQB * NBX_MAX_SPLITS * 4));
-  s.mg_scale = reinterpret_cast<float*>(take(kQB * 4));
-  s.mg_dead = reinterpret_cast<int*>(take(kQB * 4));
-  s.meta = reinterpret_cast<UnitMeta*>(take(2 * sizeof(UnitMeta)));
-  s.stage_ok = reinterpret_cast<int*>(take(C::kStages * 4));
-  s.flags = reinterpret_cast<int*>(take(4 * 4));
-  s.full = reinterpret_cast<uint64_t*>(take(C::kStages * 8));
-  s.empty = reinterpret_cast<uint64_t*>(take(C::kStages * 8));
-  s.qfull = reinterpret_cast<uint64_t*>(take(2 * 8));
-  s.qempty = reinterpret_cast<uint64_t*>(take(2 * 8));
-  s.cbar = reinterpret_cast<uint64_t*>(take(8));
-  return s;
-}
-
-template <class C, int D>
-constexpr int smem_bytes() {
-  int n = 0;
-  auto r = [](int b) { return ((b + 127) / 128) * 128; };
-  n += r(C::kStages * C::kStageBytes) + r(2 * C::kQBytes) + r(C::kRedAccBytes) + 2 * r(kConsumerWarps * kQB * 4) +
-       r(C::kPBufBytes) + 2 * r(kQB * NBX_MAX_SPLITS * 4) + 2 * r(kQB * 4) + r(2 * sizeof(UnitMeta)) +
-       r(C::kStages * 4) + r(16) + 2 * r(C::kStages * 8) + 2 * r(16) + r(8);
-  return n;
-}
+template <class C>
+struct Carver {
+  static constexpr int r(int b) { return ((b + 127) / 128) * 128; }
+  static constexpr int bytes() {
+    return r(C::kStages * C::kStageBytes) + r(2 * C::kQBytes) + r(2 * C::kRedFloats * 4) + r(C::kPBufBytes) +
+           r(2 * (int)sizeof(UnitMeta)) + r(C::kStages * 4) + r(16) + 2 * r(C::kStages * 8) + 2 * r(16) + r(8);
+  }
+  __device__ static SmemLayout carve(char* base) {
+    SmemLayout s;
+    char* p = base;
+    auto take = [&](int b) {
+      char* q = p;
+      p += r(b);
+      return q;
+    };
+    s.stages = take(C::kStages * C::kStageBytes);
+    s.qbuf = take(2 * C::kQBytes);
+    s.red = reinterpret_cast<float*>(take(2 * C::kRedFloats * 4));
+    s.pbuf = reinterpret_cast<f32x2*>(take(C::kPBufBytes));
+    s.meta = reinterpret_cast<UnitMeta*>(take(2 * sizeof(UnitMeta)));
+    s.stage_ok = reinterpret_cast<int*>(take(C::kStages * 4));
+    s.flags = reinterpret_cast<int*>(take(16));
+    s.full = reinterpret_cast<uint64_t*>(take(C::kStages * 8));
+    s.empty = reinterpret_cast<uint64_t*>(take(C::kStages * 8));
+    s.qfull = reinterpret_cast<uint64_t*>(take(16));
+    s.qempty = reinterpret_cast<uint64_t*>(take(16));
+    s.cbar = reinterpret_cast<uint64_t*>(take(8));
+    return s;
+  }
+};
 
 // Bounded wait that also gives up as soon as another warp of the CTA has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -142,63 +131,77 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0u) {
-      if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (*abort_flag) return false;
+    if ((i & 3u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// VPL consecutive elements of format PT at shared address a (aligned to VPL elements), as packed pairs.
+template <class PT, int VPL>
+__device__ __forceinline__ void lds_row_x2(uint32_t a, f32x2* out) {
+  constexpr int kBytes = VPL * PT::kBytes;
+  if constexpr (kBytes >= 16) {
+#pragma unroll
+    for (int c = 0; c < kBytes / 16; ++c) unpack16x2<PT>(lds128(a + 16 * c), out + c * (PT::kEPV / 2));
+  } else if constexpr (kBytes == 8) {
+    const uint2 v = lds64(a);
+    if constexpr (PT::kCode == NBX_F32) {
+      out[0] = (static_cast<f32x2>(v.y) << 32) | v.x;
+    } else if constexpr (PT::kCode == NBX_BF16) {
+      out[0] = bf16x2_to_f32x2(v.x);
+      out[1] = bf16x2_to_f32x2(v.y);
+    } else {
+      out[0] = e4m3x2_to_f32x2(v.x & 0xffffu);
+      out[1] = e4m3x2_to_f32x2(v.x >> 16);
+      out[2] = e4m3x2_to_f32x2(v.y & 0xffffu);
+      out[3] = e4m3x2_to_f32x2(v.y >> 16);
     }
+  } else if constexpr (kBytes == 4) {
+    const uint32_t v = lds32(a);
+    if constexpr (PT::kCode == NBX_BF16) {
+      out[0] = bf16x2_to_f32x2(v);
+    } else {
+      out[0] = e4m3x2_to_f32x2(v & 0xffffu);
+      out[1] = e4m3x2_to_f32x2(v >> 16);
+    }
+  } else {
+    out[0] = e4m3x2_to_f32x2(lds16(a));
+  }
+}
+
+// One position of P*V: acc_i += (p_i, p_i) * v for the 4 vectors, p pairs at pb, the lane's V
+// elements at va (shared addresses).
+template <class PT, int VPL>
+__device__ __forceinline__ void pv_step(uint32_t pb, uint32_t va, f32x2 (&acc2)[kQB][VPL / 2]) {
+  f32x2 p0, p1, p2, p3;
+  lds2x64(pb, p0, p1);
+  lds2x64(pb + 16, p2, p3);
+  f32x2 vf[VPL / 2];
+  lds_row_x2<PT, VPL>(va, vf);
+#pragma unroll
+  for (int k = 0; k < VPL / 2; ++k) {
+    acc2[0][k] = fma2(p0, vf[k], acc2[0][k]);
+    acc2[1][k] = fma2(p1, vf[k], acc2[1][k]);
+    acc2[2][k] = fma2(p2, vf[k], acc2[2][k]);
+    acc2[3][k] = fma2(p3, vf[k], acc2[3][k]);
   }
 }
 
 // ------------------------------------------------------------------------------------ partial
-// VPL consecutive elements of format PT at p (aligned to VPL elements), as float pairs.
-template <class PT, int VPL>
-__device__ __forceinline__ void load_row_pairs(const char* p, float2* out) {
-  constexpr int kBytes = VPL * PT::kBytes;
-  if constexpr (kBytes >= 16) {
-#pragma unroll
-    for (int c = 0; c < kBytes / 16; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(p + 16 * c);
-      unpack16<PT>(v, out + c * (PT::kEPV / 2));
-    }
-  } else if constexpr (kBytes == 8) {
-    const uint2 v = *reinterpret_cast<const uint2*>(p);
-    if constexpr (PT::kCode == NBX_F32) {
-      out[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
-    } else if constexpr (PT::kCode == NBX_BF16) {
-      out[0] = bf16x2_to_float2(v.x);
-      out[1] = bf16x2_to_float2(v.y);
-    } else {
-      out[0] = e4m3x2_to_float2(v.x & 0xffffu);
-      out[1] = e4m3x2_to_float2(v.x >> 16);
-      out[2] = e4m3x2_to_float2(v.y & 0xffffu);
-      out[3] = e4m3x2_to_float2(v.y >> 16);
-    }
-  } else if constexpr (kBytes == 4) {
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-    if constexpr (PT::kCode == NBX_BF16) {
-      out[0] = bf16x2_to_float2(v);
-    } else {
-      out[0] = e4m3x2_to_float2(v & 0xffffu);
-      out[1] = e4m3x2_to_float2(v >> 16);
-    }
-  } else {
-    out[0] = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(p));
-  }
-}
-
 template <class PT, class QT, int D>
-__global__ void __launch_bounds__(kDecodeThreads, 2) decode_partial_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBlocks)
+    decode_partial_kernel(DecodeParams p) {
   using C = DecodeCfg<PT, QT, D>;
   constexpr int NS = C::kStages;
   constexpr int LPT = C::kLPT;
-  constexpr int TG = C::kTG;
+  constexpr int TPG = C::kTPG;
   constexpr int NV = C::kNV;
   constexpr int EPV = PT::kEPV;
   constexpr int VPL = C::kVPL;
   constexpr int NW = kConsumerWarps;
 
   extern __shared__ __align__(1024) char smem_raw[];
-  SmemLayout sm = carve<C, D>(smem_raw);
+  SmemLayout sm = Carver<C>::carve(smem_raw);
   volatile int* abort_flag = sm.flags;
 
   const int warp = threadIdx.x >> 5;
@@ -220,6 +223,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_partial_kernel(Decod
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();              // the plan kernel's work list and the append's positions are visible from here on
+  pdl_launch_dependents(); // the merge kernel may be scheduled as CTAs of this grid retire
 
   const int n_units = p.header[0] * p.h_kv * p.row_blocks;
   const int unit_span = p.h_kv * p.row_blocks;
@@ -257,60 +262,89 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_partial_kernel(Decod
         mt.b = en.b;
         mt.s = en.s;
         mt.h = h;
-        mt.rb = rb;
         mt.start = en.start;
         mt.end = en.end;
         mt.n_splits = sp.n_splits;
-        mt.len = sp.len;
-        sm.meta[slot] = mt;
         const int q0 = rb * kQB;
         const int nvalid = min(kQB, RG - q0);
-        mbar_arrive_expect_tx(&sm.qfull[slot], static_cast<uint32_t>(nvalid * D * QT::kBytes));
-        for (int i = 0; i < nvalid; ++i) {
+        mt.nvec = nvalid;
+        mt.pad = 0;
+#pragma unroll
+        for (int i = 0; i < kQB; ++i) {
           const int qi = q0 + i;
           const int r = qi / p.group;
           const int g = qi - r * p.group;
-          const int64_t row = (static_cast<int64_t>(en.b) * p.rows + r) * p.h_q + static_cast<int64_t>(h) * p.group + g;
-          bulk_g2s(sm.qbuf + slot * C::kQBytes + i * D * QT::kBytes,
-                   static_cast<const char*>(p.q) + row * D * QT::kBytes, D * QT::kBytes, &sm.qfull[slot]);
+          const bool vq = i < nvalid;
+          mt.pos[i] = vq ? sp.len - p.rows + r : -1;
+          mt.orow[i] = vq ? (static_cast<int64_t>(en.b) * p.rows + r) * p.h_q + static_cast<int64_t>(h) * p.group + g
+                          : 0;
         }
+        sm.meta[slot] = mt;
+        mbar_arrive_expect_tx(&sm.qfull[slot], static_cast<uint32_t>(nvalid * D * QT::kBytes));
+        for (int i = 0; i < nvalid; ++i)
+          bulk_g2s(sm.qbuf + slot * C::kQBytes + i * D * QT::kBytes,
+                   static_cast<const char*>(p.q) + mt.orow[i] * D * QT::kBytes, D * QT::kBytes, &sm.qfull[slot]);
       }
-      // tiles of the split, page ids fetched 32 at a time by the whole warp
+      // stages of two 16-position tiles; page ids fetched 32 at a time by the whole warp
       const int P = p.page_tokens;
-      const int first_page = en.start / P;
-      const int last_page = (en.end - 1) / P;
       const int32_t* bt_row = p.block_table + static_cast<int64_t>(en.b) * p.max_pages;
-      for (int pc = first_page; pc <= last_page && ok; pc += 32) {
-        const int my_page = (pc + lane <= last_page) ? bt_row[pc + lane] : -1;
-        const int n_lo = max(en.start, pc * P);
-        const int n_hi = min(en.end, (pc + 32) * P);
-        for (int n0 = n_lo; n0 < n_hi; n0 += kTileN) {
-          const int page = __shfl_sync(0xffffffffu, my_page, n0 / P - pc);
-          if (lane == 0) {
-            const uint32_t stage = tile_seq % NS;
-            if (tile_seq >= static_cast<uint32_t>(NS))
-              ok = wait_or_abort(&sm.empty[stage], ((tile_seq / NS) - 1) & 1u, abort_flag);
-            if (ok) {
-              const bool valid = page >= 0 && page < p.num_pages;
-              sm.stage_ok[stage] = valid ? 1 : 0;
-              if (valid) {
-                const int64_t off = ((static_cast<int64_t>(page) * p.h_kv + h) * P + (n0 - (n0 / P) * P)) * D;
-                char* dst = sm.stages + stage * C::kStageBytes;
-                mbar_arrive_expect_tx(&sm.full[stage], C::kStageBytes);
-                bulk_g2s(dst, static_cast<const char*>(p.k_pool) + off * PT::kBytes, C::kTileBytes, &sm.full[stage]);
-                bulk_g2s(dst + C::kTileBytes, static_cast<const char*>(p.v_pool) + off * PT::kBytes, C::kTileBytes,
-                         &sm.full[stage]);
+      const int last_page = (en.end - 1) / P;
+      int pc = en.start / P;
+      int my_page = (pc + lane <= last_page) ? bt_row[pc + lane] : -1;
+      for (int n0 = en.start; n0 < en.end; n0 += C::kStageTok) {
+        int pages[2];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int nh = n0 + hf * kTileN;
+          const int pi = nh / P;
+          if (nh < en.end && pi >= pc + 32) {   // warp-uniform: next chunk of page ids
+            pc = pi;
+            my_page = (pc + lane <= last_page) ? bt_row[pc + lane] : -1;
+          }
+          pages[hf] = __shfl_sync(0xffffffffu, my_page, (pi - pc) & 31);
+        }
+        if (lane == 0) {
+          const uint32_t stage = tile_seq % NS;
+          if (tile_seq >= static_cast<uint32_t>(NS))
+            ok = wait_or_abort(&sm.empty[stage], ((tile_seq / NS) - 1) & 1u, abort_flag);
+          if (ok) {
+            int okbits = 0;
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int nh = n0 + hf * kTileN;
+              if (nh >= en.end) continue;
+              if (pages[hf] >= 0 && pages[hf] < p.num_pages) {
+                okbits |= 1 << hf;
+                bytes += 2 * C::kTileBytes;
               } else {
                 raise_status(p.status, NBX_DEV_BAD_PAGE);
-                mbar_arrive(&sm.full[stage]);
               }
-              sm.flags[2] = static_cast<int>(tile_seq + 1);
             }
+            sm.stage_ok[stage] = okbits;
+            char* dst = sm.stages + stage * C::kStageBytes;
+            if (bytes) {
+              mbar_arrive_expect_tx(&sm.full[stage], bytes);
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                if (!((okbits >> hf) & 1)) continue;
+                const int nh = n0 + hf * kTileN;
+                const int64_t off =
+                    ((static_cast<int64_t>(pages[hf]) * p.h_kv + h) * P + (nh - (nh / P) * P)) * D * PT::kBytes;
+                bulk_g2s(dst + hf * C::kTileBytes, static_cast<const char*>(p.k_pool) + off, C::kTileBytes,
+                         &sm.full[stage]);
+                bulk_g2s(dst + C::kHalfBytes + hf * C::kTileBytes, static_cast<const char*>(p.v_pool) + off,
+                         C::kTileBytes, &sm.full[stage]);
+              }
+            } else {
+              mbar_arrive(&sm.full[stage]);
+            }
+            sm.flags[2] = static_cast<int>(tile_seq + 1);
           }
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          ++tile_seq;
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        ++tile_seq;
       }
       ++unit_seq;
       u = __shfl_sync(0xffffffffu, u_next, 0);
@@ -329,107 +363,143 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_partial_kernel(Decod
   }
 
   // ================================================================== consumer warps
-  const int j = lane % LPT;                                  // lane within its position
-  const int tg = lane / LPT;                                 // position within the warp pass
-  const int gsel = ((j & 1) << 1) | ((j >> 1) & 1);          // vector this lane's score belongs to
-  const int ct = threadIdx.x;                                // 0 .. 127
+  const int j = lane % LPT;   // lane within its position group
+  const int tg = lane / LPT;  // position group within the warp
+  // after the transposing reduction this lane holds the score of (position tsel, vector vsel)
+  const int tsel = (TPG == 2) ? (j & 1) : 0;
+  const int vsel = (TPG == 2) ? ((((j >> 1) & 1) << 1) | ((j >> 2) & 1)) : (((j & 1) << 1) | ((j >> 1) & 1));
+  const bool p_writer = (LPT <= 8) || j < 8;   // one lane per distinct (position, vector)
+  const int ct = threadIdx.x;    // 0 .. 127
   uint32_t tile_seq = 0, unit_seq = 0, cphase = 0;
   bool ok = true;
-  // bounded barrier over the consumer threads (an mbarrier, so a warp that gave up cannot hang the others)
+  // bounded barrier over the consumer threads (an mbarrier: a warp that gave up cannot hang the others)
   auto csync = [&]() -> bool {
     mbar_arrive(sm.cbar);
     const bool r = wait_or_abort(sm.cbar, cphase & 1u, abort_flag);
     ++cphase;
     return r;
   };
-  float* pb = sm.pbuf + warp * TG * kQB;
+  // 32-bit shared addresses; per-lane offsets inside a stage are fixed for the whole kernel
+  const uint32_t stages_base = smem_u32(sm.stages);
+  const uint32_t k_lane_off = static_cast<uint32_t>(tg * TPG * D * PT::kBytes + j * 16);
+  const uint32_t v_lane_off = static_cast<uint32_t>(C::kHalfBytes + lane * VPL * PT::kBytes);
+  const uint32_t pb_addr = smem_u32(sm.pbuf + warp * C::kPassTok * kQB);
+  const uint32_t p_store = pb_addr + static_cast<uint32_t>(((tg * TPG + tsel) * kQB + vsel) * 8);
 
   for (;;) {
     const uint32_t slot = unit_seq & 1u;
-    if (!wait_or_abort(&sm.qfull[slot], (unit_seq >> 1) & 1u, abort_flag)) { ok = false; break; }
-    const UnitMeta mt = sm.meta[slot];
-    if (mt.b < 0) break;
-    const int q0 = mt.rb * kQB;
+    if (!wait_or_abort(&sm.qfull[slot], (unit_seq >> 1) & 1u, abort_flag)) {
+      ok = false;
+      break;
+    }
+    // the unit's metadata stays in its shared slot until this unit's epilogue is done
+    const UnitMeta* mtp = &sm.meta[slot];
+    const int u_b = mtp->b;
+    if (u_b < 0) break;
+    const int u_start = mtp->start, u_end = mtp->end, u_nvec = mtp->nvec;
 
     // ---- query vectors: this lane's 16 elements of each, scaled into log2 units
-    float2 q2[kQB][8];
+    f32x2 q2[kQB][8];
     {
       const char* qs = sm.qbuf + slot * C::kQBytes;
 #pragma unroll
       for (int i = 0; i < kQB; ++i) {
-        const bool vq = q0 + i < RG;
+        const bool vq = i < u_nvec;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
 #pragma unroll
           for (int e2 = 0; e2 < EPV / 2; ++e2) {
             const int el = (j + v * LPT) * EPV + 2 * e2;
-            float2 x = load_pair<QT>(qs + (i * D + el) * QT::kBytes);
-            x.x = vq ? x.x * p.qk_scale_log2 : 0.f;
-            x.y = vq ? x.y * p.qk_scale_log2 : 0.f;
-            q2[i][v * (EPV / 2) + e2] = x;
+            const float2 x = load_pair<QT>(qs + (i * D + el) * QT::kBytes);
+            q2[i][v * (EPV / 2) + e2] = vq ? pack2(x.x * p.qk_scale_log2, x.y * p.qk_scale_log2) : 0ull;
           }
         }
       }
     }
-    int pos_sel = -1;   // last visible key of vector gsel (causal window of multi-row units)
-    {
-      const int qi = q0 + gsel;
-      if (qi < RG) pos_sel = mt.len - p.rows + qi / p.group;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.qempty[slot]);
+    const int pos_sel = mtp->pos[vsel];   // last visible key of vector vsel
 
     float m_run = -INFINITY;
     float l_run = 0.f;
-    float2 acc2[kQB][VPL / 2];
+    f32x2 acc2[kQB][VPL / 2];
 #pragma unroll
     for (int i = 0; i < kQB; ++i)
 #pragma unroll
-      for (int k = 0; k < VPL / 2; ++k) acc2[i][k] = make_float2(0.f, 0.f);
+      for (int k = 0; k < VPL / 2; ++k) acc2[i][k] = 0ull;
 
-    for (int n0 = mt.start; n0 < mt.end; n0 += kTileN) {
+    const int n_stages = (u_end - u_start + C::kStageTok - 1) / C::kStageTok;
+    for (int t = 0; t < n_stages; ++t, ++tile_seq) {
       const uint32_t stage = tile_seq % NS;
-      if (!wait_or_abort(&sm.full[stage], (tile_seq / NS) & 1u, abort_flag)) { ok = false; break; }
-      if (sm.stage_ok[stage]) {
-        const char* kt = sm.stages + stage * C::kStageBytes;
-        const char* vt = kt + C::kTileBytes;
+      if (!wait_or_abort(&sm.full[stage], (tile_seq / NS) & 1u, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int okbits = sm.stage_ok[stage];
+      if (okbits) {
+        const int n0 = u_start + t * C::kStageTok;
+        const bool full_stage = (okbits == 3) && (n0 + C::kStageTok <= u_end);
+        const uint32_t st_base = stages_base + stage * C::kStageBytes;
 #pragma unroll 1
-        for (int grp = warp; grp < C::kGroups; grp += NW) {
-          const int t = grp * TG + tg;
-          const int n = n0 + t;
-          // ---- scores s_i = q_i . k_n for the 4 vectors, partial over this lane's elements
-          float2 s2[kQB];
+        for (int pass = 0; pass < C::kWarpPasses; ++pass) {
+          const int pbase = warp * C::kWarpTok + pass * C::kPassTok;   // first position of this pass in the stage
+          // ---- scores s[tk][i] = q_i . k for this lane group's TPG positions, partial over 16 elements
+          f32x2 s2[TPG][kQB];
 #pragma unroll
-          for (int i = 0; i < kQB; ++i) s2[i] = make_float2(0.f, 0.f);
+          for (int tk = 0; tk < TPG; ++tk)
 #pragma unroll
-          for (int v = 0; v < NV; ++v) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(kt + t * D * PT::kBytes + (j + v * LPT) * 16);
-            float2 kf[EPV / 2];
-            unpack16<PT>(kv, kf);
+            for (int i = 0; i < kQB; ++i) s2[tk][i] = 0ull;
 #pragma unroll
-            for (int e2 = 0; e2 < EPV / 2; ++e2)
+          for (int tk = 0; tk < TPG; ++tk) {
 #pragma unroll
-              for (int i = 0; i < kQB; ++i) s2[i] = ffma2(q2[i][v * (EPV / 2) + e2], kf[e2], s2[i]);
+            for (int v = 0; v < NV; ++v) {
+              const uint4 kv = lds128(st_base + (pbase + tk) * D * PT::kBytes + k_lane_off + v * LPT * 16);
+              f32x2 kf[EPV / 2];
+              unpack16x2<PT>(kv, kf);
+#pragma unroll
+              for (int e2 = 0; e2 < EPV / 2; ++e2)
+#pragma unroll
+                for (int i = 0; i < kQB; ++i) s2[tk][i] = fma2(q2[i][v * (EPV / 2) + e2], kf[e2], s2[tk][i]);
+            }
           }
-          const float s0 = s2[0].x + s2[0].y, s1 = s2[1].x + s2[1].y;
-          const float s2v = s2[2].x + s2[2].y, s3 = s2[3].x + s2[3].y;
-          // ---- transposing reduction over the LPT lanes of this position
-          const bool b0 = j & 1;
-          float k0 = b0 ? s2v : s0, k1 = b0 ? s3 : s1;
-          k0 += __shfl_xor_sync(0xffffffffu, b0 ? s0 : s2v, 1);
-          k1 += __shfl_xor_sync(0xffffffffu, b0 ? s1 : s3, 1);
-          const bool b1 = (j >> 1) & 1;
-          float mine = b1 ? k1 : k0;
-          mine += __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
+          float sv[TPG][kQB];
 #pragma unroll
-          for (int off = 4; off < LPT; off <<= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
-          const bool valid = (n < mt.end) && (n <= pos_sel);
+          for (int tk = 0; tk < TPG; ++tk)
+#pragma unroll
+            for (int i = 0; i < kQB; ++i) {
+              const float2 t2 = unpack2(s2[tk][i]);
+              sv[tk][i] = t2.x + t2.y;
+            }
+          // ---- transposing reduction over the LPT lanes of a position group
+          float mine;
+          if constexpr (TPG == 2) {
+            const bool b0 = j & 1;   // keep position b0, send the other
+            float a[kQB];
+#pragma unroll
+            for (int i = 0; i < kQB; ++i)
+              a[i] = (b0 ? sv[1][i] : sv[0][i]) + __shfl_xor_sync(0xffffffffu, b0 ? sv[0][i] : sv[1][i], 1);
+            const bool b1 = (j >> 1) & 1;   // keep vectors 2*b1, 2*b1+1
+            const float c0 = (b1 ? a[2] : a[0]) + __shfl_xor_sync(0xffffffffu, b1 ? a[0] : a[2], 2);
+            const float c1 = (b1 ? a[3] : a[1]) + __shfl_xor_sync(0xffffffffu, b1 ? a[1] : a[3], 2);
+            const bool b2 = (j >> 2) & 1;   // keep vector 2*b1 + b2
+            mine = (b2 ? c1 : c0) + __shfl_xor_sync(0xffffffffu, b2 ? c0 : c1, 4);
+            if constexpr (LPT == 16) mine += __shfl_xor_sync(0xffffffffu, mine, 8);
+          } else {
+            const bool b0 = j & 1;   // keep vectors 2*b0, 2*b0+1
+            const float k0 = (b0 ? sv[0][2] : sv[0][0]) + __shfl_xor_sync(0xffffffffu, b0 ? sv[0][0] : sv[0][2], 1);
+            const float k1 = (b0 ? sv[0][3] : sv[0][1]) + __shfl_xor_sync(0xffffffffu, b0 ? sv[0][1] : sv[0][3], 1);
+            const bool b1 = (j >> 1) & 1;   // keep vector 2*b0 + b1
+            mine = (b1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
+          }
+          const int rs = pbase + tg * TPG + tsel;   // this lane's position inside the stage
+          const int n = n0 + rs;
+          const bool valid = ((okbits >> (rs / kTileN)) & 1) && (n < u_end) && (n <= pos_sel);
           const float s = valid ? mine : -INFINITY;
-          // ---- online softmax, lazy rescale
+          // ---- online softmax, lazy rescale; the max runs over the lanes holding the same vector
+          // (NaN-propagating max: a NaN score makes the running max NaN, so it reaches the output)
           float mx = s;
+          if constexpr (TPG == 2) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
 #pragma unroll
-          for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          const bool need = mx > m_run + kTau;
+          for (int off = LPT; off < 32; off <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          const bool need = !(mx <= m_run + kTau);
           if (__any_sync(0xffffffffu, need)) {
             const float m_new = need ? mx : m_run;
             const float f = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
@@ -437,86 +507,86 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_partial_kernel(Decod
             l_run *= f;
 #pragma unroll
             for (int i = 0; i < kQB; ++i) {
-              const float fi = __shfl_sync(0xffffffffu, f, ((i & 1) << 1) | (i >> 1));
+              const int src = (TPG == 2) ? (((i >> 1) << 1) | ((i & 1) << 2)) : (((i & 1) << 1) | (i >> 1));
+              const float fi = __shfl_sync(0xffffffffu, f, src);
+              const f32x2 fi2 = pack2(fi, fi);
 #pragma unroll
-              for (int k = 0; k < VPL / 2; ++k) acc2[i][k] = fmul2(acc2[i][k], make_float2(fi, fi));
+              for (int k = 0; k < VPL / 2; ++k) acc2[i][k] = mul2(acc2[i][k], fi2);
             }
           }
           const float pw = valid ? fast_exp2(s - m_run) : 0.f;
           l_run += pw;
-          if (j < 4) pb[tg * kQB + gsel] = pw;
+          if (p_writer) sts64(p_store, pack2(pw, pw));
           __syncwarp();
-          // ---- acc_i += p_i,n * v_n over this pass's positions
+          // ---- acc_i += p_i,n * v_n over this pass's positions (no per-position test in full stages)
+          if (full_stage) {
 #pragma unroll
-          for (int tt = 0; tt < TG; ++tt) {
-            const int trow = grp * TG + tt;
-            if (n0 + trow < mt.end) {
-              const float4 pv = *reinterpret_cast<const float4*>(pb + tt * kQB);
-              float2 vf[VPL / 2];
-              load_row_pairs<PT, VPL>(vt + (trow * D + lane * VPL) * PT::kBytes, vf);
+            for (int pt = 0; pt < C::kPassTok; ++pt)
+              pv_step<PT, VPL>(pb_addr + pt * kQB * 8, st_base + v_lane_off + (pbase + pt) * D * PT::kBytes, acc2);
+          } else {
 #pragma unroll
-              for (int k = 0; k < VPL / 2; ++k) {
-                acc2[0][k] = ffma2(make_float2(pv.x, pv.x), vf[k], acc2[0][k]);
-                acc2[1][k] = ffma2(make_float2(pv.y, pv.y), vf[k], acc2[1][k]);
-                acc2[2][k] = ffma2(make_float2(pv.z, pv.z), vf[k], acc2[2][k]);
-                acc2[3][k] = ffma2(make_float2(pv.w, pv.w), vf[k], acc2[3][k]);
-              }
-            }
+            for (int pt = 0; pt < C::kPassTok; ++pt)
+              if (((okbits >> ((pbase + pt) / kTileN)) & 1) && n0 + pbase + pt < u_end)
+                pv_step<PT, VPL>(pb_addr + pt * kQB * 8, st_base + v_lane_off + (pbase + pt) * D * PT::kBytes, acc2);
           }
           __syncwarp();
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[stage]);
-      ++tile_seq;
     }
     if (!ok) break;
 
-    // ---- epilogue: merge the four warps' states in warp order
+    // ---- epilogue: merge the four warps' states in warp order (double-buffered scratch)
+    float* red = sm.red + slot * C::kRedFloats;
     {
       float l_tot = l_run;
+      if constexpr (TPG == 2) l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
 #pragma unroll
       for (int off = LPT; off < 32; off <<= 1) l_tot += __shfl_xor_sync(0xffffffffu, l_tot, off);
-      if (lane < 4) {
-        sm.red_m[warp * kQB + gsel] = m_run;
-        sm.red_l[warp * kQB + gsel] = l_tot;
+      float* rw = red + warp * (kQB * D + 2 * kQB);
+      if (lane < 8 && tsel == 0) {   // one lane per vector
+        rw[kQB * D + vsel] = m_run;
+        rw[kQB * D + kQB + vsel] = l_tot;
       }
-      float* ra = sm.red_acc + warp * kQB * D;
 #pragma unroll
       for (int i = 0; i < kQB; ++i)
 #pragma unroll
-        for (int k = 0; k < VPL / 2; ++k)
-          *reinterpret_cast<float2*>(ra + i * D + lane * VPL + 2 * k) = acc2[i][k];
+        for (int k = 0; k < VPL / 2; ++k) *reinterpret_cast<f32x2*>(rw + i * D + lane * VPL + 2 * k) = acc2[i][k];
     }
-    if (!csync()) { ok = false; break; }
-    const bool multi = mt.n_splits > 1;
-    for (int o = ct; o < kQB * D; o += NW * 32) {
+    if (!csync()) {
+      ok = false;
+      break;
+    }
+    const bool multi = mtp->n_splits > 1;
+    const int u_split = mtp->s;
+#pragma unroll
+    for (int x = 0; x < kQB * D / (NW * 32); ++x) {
+      const int o = ct + x * NW * 32;
       const int i = o / D;
       const int dd = o - i * D;
-      const int qi = q0 + i;
-      if (qi >= RG) continue;
+      if (i >= u_nvec) continue;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.red_m[w * kQB + i]);
+      for (int w = 0; w < NW; ++w) M = max_nan(M, red[w * (kQB * D + 2 * kQB) + kQB * D + i]);
       float L = 0.f, A = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-          const float mw = sm.red_m[w * kQB + i];
+          const float* rw = red + w * (kQB * D + 2 * kQB);
+          const float mw = rw[kQB * D + i];
           if (mw != -INFINITY) {
             const float f = fast_exp2(mw - M);
-            L += f * sm.red_l[w * kQB + i];
-            A += f * sm.red_acc[(w * kQB + i) * D + dd];
+            L += f * rw[kQB * D + kQB + i];
+            A += f * rw[i * D + dd];
           }
         }
       }
-      const int r = qi / p.group;
-      const int g = qi - r * p.group;
-      const int64_t orow = (static_cast<int64_t>(mt.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mt.h) * p.group + g;
+      const int64_t orow = mtp->orow[i];
       if (!multi) {
         p.out[orow * D + dd] = (M == -INFINITY) ? 0.f : A * (p.v_scale / L);
       } else {
-        const int64_t prow = orow * p.max_splits + mt.s;
+        const int64_t prow = orow * p.max_splits + u_split;
         p.acc_part[prow * D + dd] = A;
         if (dd == 0) {
           p.m_part[prow] = M;
@@ -524,70 +594,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_partial_kernel(Decod
         }
       }
     }
-    if (multi) {
-      __threadfence();
-      if (!csync()) { ok = false; break; }
-      if (ct == 0) {
-        const int64_t tk = (static_cast<int64_t>(mt.b) * p.h_kv + mt.h) * p.row_blocks + mt.rb;
-        const int old = atomicAdd(&p.tickets[tk], 1);
-        sm.flags[1] = (old == mt.n_splits - 1) ? 1 : 0;
-      }
-      if (!csync()) { ok = false; break; }
-      if (sm.flags[1]) {
-        // ---- last split of this (sequence, KV head, row block) to finish: merge in split order
-        __threadfence();
-        const int S = mt.n_splits;
-        for (int x = ct; x < kQB * S; x += NW * 32) {
-          const int i = x / S;
-          const int s = x - i * S;
-          const int qi = q0 + i;
-          float mv = -INFINITY, lv = 0.f;
-          if (qi < RG) {
-            const int r = qi / p.group;
-            const int g = qi - r * p.group;
-            const int64_t orow =
-                (static_cast<int64_t>(mt.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mt.h) * p.group + g;
-            mv = ld_cg_f32(p.m_part + orow * p.max_splits + s);
-            lv = ld_cg_f32(p.l_part + orow * p.max_splits + s);
-          }
-          sm.mg_m[i * NBX_MAX_SPLITS + s] = mv;
-          sm.mg_w[i * NBX_MAX_SPLITS + s] = lv;
-        }
-        if (!csync()) { ok = false; break; }
-        if (ct < kQB) {
-          const int i = ct;
-          float M = -INFINITY;
-          for (int s = 0; s < S; ++s) M = fmaxf(M, sm.mg_m[i * NBX_MAX_SPLITS + s]);
-          float L = 0.f;
-          for (int s = 0; s < S; ++s) {
-            const float mv = sm.mg_m[i * NBX_MAX_SPLITS + s];
-            const float w = (mv == -INFINITY) ? 0.f : fast_exp2(mv - M);
-            L += w * sm.mg_w[i * NBX_MAX_SPLITS + s];
-            sm.mg_w[i * NBX_MAX_SPLITS + s] = w;
-          }
-          sm.mg_dead[i] = (M == -INFINITY) ? 1 : 0;
-          sm.mg_scale[i] = p.v_scale / L;
-        }
-        if (!csync()) { ok = false; break; }
-        for (int o = ct; o < kQB * D; o += NW * 32) {
-          const int i = o / D;
-          const int dd = o - i * D;
-          const int qi = q0 + i;
-          if (qi >= RG) continue;
-          const int r = qi / p.group;
-          const int g = qi - r * p.group;
-          const int64_t orow =
-              (static_cast<int64_t>(mt.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mt.h) * p.group + g;
-          float A = 0.f;
-          for (int s = 0; s < S; ++s) {
-            if (sm.mg_m[i * NBX_MAX_SPLITS + s] == -INFINITY) continue;
-            A += sm.mg_w[i * NBX_MAX_SPLITS + s] * ld_cg_f32(p.acc_part + (orow * p.max_splits + s) * D + dd);
-          }
-          p.out[orow * D + dd] = sm.mg_dead[i] ? 0.f : A * sm.mg_scale[i];
-        }
-      }
-    }
-    if (!csync()) { ok = false; break; }   // shared scratch is reused by the next unit
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.qempty[slot]);   // the slot's queries and metadata are free again
     ++unit_seq;
   }
 
@@ -608,8 +616,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_partial_kernel(Decod
 template <class PT, class QT, int D>
 cudaError_t launch_decode(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
   using C = DecodeCfg<PT, QT, D>;
-  constexpr int smem = smem_bytes<C, D>();
-  static_assert(smem <= 227 * 1024, "shared memory per CTA");
+  constexpr int smem = Carver<C>::bytes();
+  static_assert(smem <= C::kSmemPerCta, "shared memory per CTA");
   const DeviceInfo& di = device_info();
   static int configured_for = -1;
   if (configured_for != di.device) {
@@ -619,12 +627,11 @@ cudaError_t launch_decode(const DecodeParams& p, int grid_limit, cudaStream_t st
     configured_for = di.device;
   }
   const int64_t upper = static_cast<int64_t>(p.batch) * p.max_splits * p.h_kv * p.row_blocks;
-  int64_t grid = static_cast<int64_t>(di.sm_count) * 2;
+  int64_t grid = static_cast<int64_t>(di.sm_count) * C::kMinBlocks;
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
-  decode_partial_kernel<PT, QT, D><<<static_cast<unsigned>(grid), kDecodeThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_partial_kernel<PT, QT, D>, static_cast<unsigned>(grid), kDecodeThreads, smem, stream, p);
 }
 
 #define NBX_DECODE_FOR_POOL(PT)                                                                                   \

@@ -8,7 +8,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
-#include "../../include/nbx.h"
+#include "nbx.h"
 
 namespace nbx {
 
@@ -90,30 +90,87 @@ __device__ __forceinline__ float2 load_pair<E4M3>(const void* p) {
 }
 
 // ---------------------------------------------------------------- packed fp32 math
-// Blackwell executes two fp32 FMAs per instruction on register pairs (fma.rn.f32x2).
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+// Blackwell executes two fp32 FMAs per instruction on a 64-bit register pair (fma.rn.f32x2).
+// f32x2 holds such a pair (low half = element 0); keeping pairs in 64-bit registers through
+// the hot loops avoids repacking around every packed instruction.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// two bf16 (low half = element 0) -> packed fp32 pair
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w) {
+  f32x2 r;
+  // low half: byte permute (bytes 0,1 of w to bytes 2,3, zeros below); high half: mask
+  asm("{\n\t.reg .b32 lo, hi;\n\tprmt.b32 lo, %1, 0, 0x1044;\n\tand.b32 hi, %1, 0xffff0000;\n\tmov.b64 %0, {lo, hi};\n\t}"
+      : "=l"(r)
+      : "r"(w));
+  return r;
+}
+__device__ __forceinline__ f32x2 e4m3x2_to_f32x2(uint32_t pair16) {
+  const float2 f = e4m3x2_to_float2(pair16);
+  return pack2(f.x, f.y);
+}
+
+// Unpack the 16-byte vector `v` of format T into packed pairs: out[k] holds elements 2k, 2k+1.
+template <class T>
+__device__ __forceinline__ void unpack16x2(const uint4& v, f32x2* out);
+template <>
+__device__ __forceinline__ void unpack16x2<F32>(const uint4& v, f32x2* out) {
+  out[0] = (static_cast<f32x2>(v.y) << 32) | v.x;
+  out[1] = (static_cast<f32x2>(v.w) << 32) | v.z;
+}
+template <>
+__device__ __forceinline__ void unpack16x2<BF16>(const uint4& v, f32x2* out) {
+  out[0] = bf16x2_to_f32x2(v.x);
+  out[1] = bf16x2_to_f32x2(v.y);
+  out[2] = bf16x2_to_f32x2(v.z);
+  out[3] = bf16x2_to_f32x2(v.w);
+}
+template <>
+__device__ __forceinline__ void unpack16x2<E4M3>(const uint4& v, f32x2* out) {
+  out[0] = e4m3x2_to_f32x2(v.x & 0xffffu);
+  out[1] = e4m3x2_to_f32x2(v.x >> 16);
+  out[2] = e4m3x2_to_f32x2(v.y & 0xffffu);
+  out[3] = e4m3x2_to_f32x2(v.y >> 16);
+  out[4] = e4m3x2_to_f32x2(v.z & 0xffffu);
+  out[5] = e4m3x2_to_f32x2(v.z >> 16);
+  out[6] = e4m3x2_to_f32x2(v.w & 0xffffu);
+  out[7] = e4m3x2_to_f32x2(v.w >> 16);
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its prologue early /
+// wait until the kernel this one depends on has finished and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// max that returns NaN if either input is NaN (fmaxf would drop it)
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22; ex2(-inf) = +0).
@@ -131,6 +188,35 @@ __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
 // ---------------------------------------------------------------- mbarrier + bulk copy
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Explicit shared-memory accesses on 32-bit shared addresses (volatile: they must stay behind
+// the barrier waits that publish the data).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void lds2x64(uint32_t a, unsigned long long& x, unsigned long long& y) {
+  asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "r"(a));
+}
+__device__ __forceinline__ void sts64(uint32_t a, unsigned long long v) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -151,14 +237,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed is suspended until it
+// completes (or the hint expires) instead of spinning, so waiting warps leave the issue slots free.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -178,7 +268,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
+    if ((i & 3u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/nbx.h"
+#include "nbx.h"
 
 namespace nbx {
 
@@ -58,7 +58,6 @@ struct WorkspaceLayout {
   size_t header;    // int32[64]: [0] entries in the list, [1] work counter
   size_t plan;      // SeqPlan[batch]
   size_t entries;   // Entry[batch * max_splits]
-  size_t tickets;   // int32[batch * h_kv * row_blocks]
   size_t m_part;    // f32[batch * rows * h_q * max_splits]   (log2 units)
   size_t l_part;    // f32[batch * rows * h_q * max_splits]
   size_t acc_part;  // f32[batch * rows * h_q * max_splits * d]
@@ -84,7 +83,6 @@ struct DecodeParams {
   int32_t* header;
   SeqPlan* plan;
   Entry* entries;
-  int32_t* tickets;
   float* m_part;
   float* l_part;
   float* acc_part;
@@ -95,6 +93,24 @@ struct DecodeParams {
 };
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);
+
+// Launch with programmatic dependent launch: the grid may start while the previous kernel in the
+// stream finishes; the kernel orders itself after it with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 struct MergeParams {
   const float* acc_part;

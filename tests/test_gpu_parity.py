@@ -161,6 +161,18 @@ def test_nan_key_reaches_the_output():
     assert np.all(np.isfinite(o[0, 0, G:])) and np.all(np.isfinite(o[1]))
 
 
+def test_split_of_only_nan_keys_reaches_the_output():
+    # every key of the second split is NaN: its running max is NaN, and the merge keeps it
+    case = wl.make_case("single_row_small", device=DEV, lens=[300, 40])
+    lo = int(case.tok_offset[0])
+    case.k_raw[lo + 160:lo + 300, 1, :] = float("nan")
+    sess, out = run_step(case)
+    o = out.cpu().numpy()
+    G = case.cfg.group
+    assert np.all(np.isnan(o[0, 0, G:2 * G]))
+    assert np.all(np.isfinite(o[0, 0, :G])) and np.all(np.isfinite(o[1]))
+
+
 def test_bad_page_id_sets_status_and_skips():
     case = wl.make_case("single_row_small", device=DEV, lens=[100, 600])
     sess = bench.session_for_case(case, DEV)
@@ -168,7 +180,7 @@ def test_bad_page_id_sets_status_and_skips():
     bt[1, 3] = -1
     bt[1, 5] = case.num_pages + 7
     sess.block_table = bt
-    out = sess.decode()
+    out = sess.step()
     torch.cuda.synchronize()
     assert sess.status_bits() & nbx.DEV_BAD_PAGE
     kp, vp = pins.oracle_pools(case)
@@ -181,7 +193,7 @@ def test_bad_length_sets_status():
     case = wl.make_case("single_row_small", device=DEV, lens=[100, 200])
     sess = bench.session_for_case(case, DEV)
     sess.seq_lens = torch.tensor([100, 10_000], dtype=torch.int32, device=DEV)
-    out = sess.decode()
+    out = sess.step()
     torch.cuda.synchronize()
     assert sess.status_bits() & nbx.DEV_BAD_LEN
     assert torch.all(out[1] == 0)
