@@ -159,6 +159,31 @@ NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int row
 NBX_API int nbx_paged_decode_merge(const float* acc_part, const float* m_part, const float* l_part, int n_rows,
                                    int splits, int d, float* out, void* stream);
 
+/* Bytes of device scratch that libnbx keeps for nbx_paged_decode_attn_noalloc (32 MiB). */
+#define NBX_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * nbx_paged_decode_attn_noalloc -- nbx_paged_decode_attn without a caller workspace.
+ * The pages have no counterpart of this call: it exists for callers that cannot allocate device
+ * memory (code running where cudaMalloc is not allowed, such as an allocator's own callbacks, a
+ * process whose memory budget is fixed before the library loads, or a plug-in without access to
+ * the host application's allocator).
+ *
+ * Same arguments, layouts and results as nbx_paged_decode_attn, minus workspace and
+ * workspace_bytes. The scratch is a fixed array of NBX_NOALLOC_SCRATCH_BYTES in the library's
+ * own device memory, held by every GPU that loads the library until the process exits. Sizes
+ * whose workspace (nbx_paged_decode_workspace_bytes) exceeds it return NBX_ERR_WORKSPACE without
+ * a launch. Nothing is allocated or freed.
+ * The first call on a device looks up the array's device address with that device current; make
+ * that first call before any stream capture. All calls share the one array and it keeps the last
+ * call's contents (every call rewrites what it reads), so calls that overlap on the GPU race.
+ */
+NBX_API int nbx_paged_decode_attn_noalloc(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
+                                          const void* k_pool, const void* v_pool, int pool_dtype, int num_pages,
+                                          int h_kv, int page_tokens, const int32_t* block_table, int max_pages,
+                                          const int32_t* seq_lens, int max_seq_len, float scale, float k_scale,
+                                          float v_scale, float* out, int32_t* status, void* stream);
+
 /*
  * nbx_set_decode_grid_limit -- cap the number of CTAs nbx_paged_decode_attn launches (0 = the
  * default, two per SM). Process-wide; the output is bit-identical for every value.
