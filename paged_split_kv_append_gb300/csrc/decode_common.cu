@@ -4,8 +4,8 @@
 
 namespace nbx {
 
-constexpr int kPlanThreads = 1024;
-constexpr int kSortMax = 2048;   // batches up to this size are ordered longest split first
+constexpr int kPlanThreads = 256;
+constexpr int kSortMax = 2048;   // batches up to this size are planned in shared memory, longest split first
 
 int splits_for(int length) {
   const int l = length < 1 ? 1 : length;
@@ -40,21 +40,27 @@ bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq
 
 // Reads the device lengths, writes every sequence's plan (len, positions per split, non-empty
 // splits), zeroes the work counter, writes 0 to the output rows of empty sequences, and writes
-// the work list of (sequence, split) entries: sequences with the longest splits first, splits
-// ascending.
+// the work list of (sequence, split) entries: sequences with the longest splits first (stable),
+// splits ascending. Batches above kSortMax keep their own order and take a slower serial path.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
-  __shared__ int s_key[kSortMax];
-  __shared__ int s_order[kSortMax];
-  __shared__ int s_cnt[kSortMax];
-  __shared__ int s_seg[kSortMax];
   __shared__ int s_len[kSortMax];
+  __shared__ int s_seg[kSortMax];
+  __shared__ int s_n[kSortMax];
+  __shared__ int s_order[kSortMax];
+  __shared__ int s_base[kSortMax + 1];
   __shared__ int s_warp[kPlanThreads / 32];
-  __shared__ int s_total;
+  __shared__ int s_empty;
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int B = p.batch;
   const int64_t cap = static_cast<int64_t>(p.max_pages) * p.page_tokens;
-  const bool sorted = B <= kSortMax;
+  const bool small = B <= kSortMax;
   pdl_launch_dependents();   // the partial kernel may start its prologue now; it waits for this grid
+  if (tid == 0) {
+    s_empty = 0;
+    p.header[1] = 0;
+  }
+  __syncthreads();
   for (int b = tid; b < B; b += kPlanThreads) {
     int L = p.seq_lens[b];
     if (L < 0 || L > p.max_seq_len || static_cast<int64_t>(L) > cap) {
@@ -72,42 +78,59 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
     sp.n_splits = n;
     sp.pad = 0;
     p.plan[b] = sp;
-    if (sorted) {
-      s_key[b] = n > 0 ? seg : -1;
-      s_cnt[b] = n;
-      s_seg[b] = seg;
+    if (n == 0) s_empty = 1;
+    if (small) {
       s_len[b] = L;
+      s_seg[b] = seg;
+      s_n[b] = n;
     }
   }
-  if (tid == 0) p.header[1] = 0;
   __syncthreads();
   // a sequence with no position to read gets no work unit: its rows are written here (0)
-  const int64_t row_vec4 = static_cast<int64_t>(p.rows) * p.h_q * p.d / 4;
-  for (int b = 0; b < B; ++b) {
-    if ((sorted ? s_cnt[b] : p.plan[b].n_splits) != 0) continue;
-    float4* o = reinterpret_cast<float4*>(p.out) + b * row_vec4;
-    for (int64_t x = tid; x < row_vec4; x += kPlanThreads) o[x] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  if (sorted) {
-    for (int b = tid; b < B; b += kPlanThreads) {
-      const int k = s_key[b];
-      int rank = 0;
-      for (int c = 0; c < B; ++c) {
-        const int kc = s_key[c];
-        rank += (kc > k) || (kc == k && c < b);
-      }
-      s_order[rank] = b;
+  if (s_empty) {
+    const int64_t row_vec4 = static_cast<int64_t>(p.rows) * p.h_q * p.d / 4;
+    for (int b = 0; b < B; ++b) {
+      if ((small ? s_n[b] : p.plan[b].n_splits) != 0) continue;
+      float4* o = reinterpret_cast<float4*>(p.out) + b * row_vec4;
+      for (int64_t x = tid; x < row_vec4; x += kPlanThreads) o[x] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    __syncthreads();
-    for (int i = tid; i < B; i += kPlanThreads) s_key[i] = s_cnt[s_order[i]];   // counts in list order
-    __syncthreads();
   }
-  // exclusive scan of the split counts in list order: each thread a contiguous run, then a block scan
+  if (!small) {
+    // large batch: batch order, one thread writes the whole list
+    if (tid == 0) {
+      int base = 0;
+      for (int b = 0; b < B; ++b) {
+        const SeqPlan sp = p.plan[b];
+        for (int s = 0; s < sp.n_splits; ++s) {
+          Entry e;
+          e.b = b;
+          e.s = s;
+          e.start = s * sp.seg;
+          e.end = min((s + 1) * sp.seg, sp.len);
+          p.entries[base + s] = e;
+        }
+        base += sp.n_splits;
+      }
+      p.header[0] = base;
+    }
+    return;
+  }
+  // stable rank by split length, longest first (empty sequences last)
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int k = s_n[b] > 0 ? s_seg[b] : -1;
+    int rank = 0;
+    for (int c = 0; c < B; ++c) {
+      const int kc = s_n[c] > 0 ? s_seg[c] : -1;
+      rank += (kc > k) || (kc == k && c < b);
+    }
+    s_order[rank] = b;
+  }
+  __syncthreads();
+  // exclusive scan of the split counts in list order (a contiguous run per thread, then a block scan)
   const int per = (B + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(B, tid * per), hi = min(B, lo + per);
   int run = 0;
-  for (int i = lo; i < hi; ++i) run += sorted ? s_key[i] : p.plan[i].n_splits;
-  const int lane = tid & 31, warp = tid >> 5;
+  for (int i = lo; i < hi; ++i) run += s_n[s_order[i]];
   int x = run;
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -116,40 +139,39 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   if (lane == 31) s_warp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = s_warp[lane];
+    int w = lane < kPlanThreads / 32 ? s_warp[lane] : 0;
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    s_warp[lane] = w;
-    if (lane == 31) s_total = w;
+    if (lane < kPlanThreads / 32) s_warp[lane] = w;
   }
   __syncthreads();
   int base = x - run + (warp > 0 ? s_warp[warp - 1] : 0);
   for (int i = lo; i < hi; ++i) {
-    const int b = sorted ? s_order[i] : i;
-    int n, seg, len;
-    if (sorted) {
-      n = s_cnt[b];
-      seg = s_seg[b];
-      len = s_len[b];
-    } else {
-      const SeqPlan sp = p.plan[b];
-      n = sp.n_splits;
-      seg = sp.seg;
-      len = sp.len;
-    }
-    for (int s = 0; s < n; ++s) {
-      Entry e;
-      e.b = b;
-      e.s = s;
-      e.start = s * seg;
-      e.end = min((s + 1) * seg, len);
-      p.entries[base + s] = e;
-    }
-    base += n;
+    s_base[i] = base;
+    base += s_n[s_order[i]];
   }
-  if (tid == 0) p.header[0] = s_total;
+  if (tid == kPlanThreads - 1) s_base[B] = x + (warp > 0 ? s_warp[warp - 1] : 0);
+  __syncthreads();
+  // the entries, in parallel: entry e belongs to the list position i with s_base[i] <= e < s_base[i+1]
+  const int total = s_base[B];
+  for (int e = tid; e < total; e += kPlanThreads) {
+    int l = 0, r = B - 1;
+    while (l < r) {
+      const int m = (l + r + 1) >> 1;
+      if (s_base[m] <= e) l = m; else r = m - 1;
+    }
+    const int b = s_order[l];
+    const int s = e - s_base[l];
+    Entry en;
+    en.b = b;
+    en.s = s;
+    en.start = s * s_seg[b];
+    en.end = min((s + 1) * s_seg[b], s_len[b]);
+    p.entries[e] = en;
+  }
+  if (tid == 0) p.header[0] = total;
 }
 
 // ------------------------------------------------------------------------------------ standalone merge
@@ -204,13 +226,12 @@ constexpr int kDecodeMergeThreads = 128;
 // out = v_scale * sum_s w_s acc_s / sum_s w_s l_s, s ascending. One-split sequences were written
 // by the partial kernel.
 __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(DecodeParams p) {
-  __shared__ float s_m[kQB][NBX_MAX_SPLITS];
-  __shared__ float s_l[kQB][NBX_MAX_SPLITS];
+  __shared__ float s_w[kQB][NBX_MAX_SPLITS];   // weight of each live split, -1 for a split with no visible key
   __shared__ float s_scale[kQB];
   __shared__ int s_dead[kQB];
-  __shared__ long long s_orow[kQB];
   pdl_wait();   // every partial of the decode is written and visible from here on
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const int RG = p.rows * p.group;
   const int per_seq = p.h_kv * p.row_blocks;
   const int n_groups = p.batch * per_seq;
@@ -219,60 +240,67 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
     const int rem = gi - b * per_seq;
     const int h = rem / p.row_blocks;
     const int rb = rem - h * p.row_blocks;
-    const int S = p.plan[b].n_splits;
-    if (S <= 1) continue;
     const int q0 = rb * kQB;
     const int nvec = min(kQB, RG - q0);
-    if (tid < nvec) {
-      const int qi = q0 + tid;
+    const int S = p.plan[b].n_splits;
+    if (S <= 1) continue;   // one split: the partial kernel wrote the output
+    // warp i: vector i's split weights. Lanes hold splits lane and lane + 32; max and sums are
+    // butterfly reductions, a fixed order.
+    if (warp < nvec) {
+      const int qi = q0 + warp;
       const int r = qi / p.group;
       const int g = qi - r * p.group;
-      s_orow[tid] = (static_cast<long long>(b) * p.rows + r) * p.h_q + static_cast<long long>(h) * p.group + g;
-    }
-    __syncthreads();
-    // every (vector, split) pair's m and l, one load each
-    for (int x = tid; x < nvec * S; x += kDecodeMergeThreads) {
-      const int i = x / S;
-      const int sp = x - i * S;
-      const long long row = s_orow[i] * p.max_splits + sp;
-      s_m[i][sp] = p.m_part[row];
-      s_l[i][sp] = p.l_part[row];
-    }
-    __syncthreads();
-    if (tid < nvec) {
-      float M = -INFINITY;
-      for (int sp = 0; sp < S; ++sp) M = max_nan(M, s_m[tid][sp]);
-      float L = 0.f;
-      for (int sp = 0; sp < S; ++sp) {
-        const float ms = s_m[tid][sp];
-        const bool lv = ms != -INFINITY;
-        const float w = lv ? fast_exp2(ms - M) : 0.f;
-        if (lv) L += w * s_l[tid][sp];
-        s_m[tid][sp] = lv ? w : -1.f;   // -1 marks a split with no visible key
+      const long long orow = (static_cast<long long>(b) * p.rows + r) * p.h_q + static_cast<long long>(h) * p.group + g;
+      const float* m = p.m_part + orow * p.max_splits;
+      const float* l = p.l_part + orow * p.max_splits;
+      float mv[2], lv[2];
+      bool live[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int sp = lane + 32 * k;
+        mv[k] = sp < S ? m[sp] : -INFINITY;
+        lv[k] = sp < S ? l[sp] : 0.f;
+        live[k] = mv[k] != -INFINITY;
       }
-      s_dead[tid] = (M == -INFINITY) ? 1 : 0;
-      s_scale[tid] = p.v_scale / L;
+      float M = max_nan(mv[0], mv[1]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float L = 0.f;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float w = live[k] ? fast_exp2(mv[k] - M) : 0.f;
+        if (live[k]) L += w * lv[k];
+        if (lane + 32 * k < NBX_MAX_SPLITS) s_w[warp][lane + 32 * k] = live[k] ? w : -1.f;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (lane == 0) {
+        s_dead[warp] = (M == -INFINITY) ? 1 : 0;
+        s_scale[warp] = p.v_scale / L;
+      }
     }
     __syncthreads();
-    // each thread a float4 of one vector's output; 16 splits' loads in flight per batch, summed in
+    // each thread a float4 of one vector's output, every split's load in flight, summed in
     // ascending split order
     const int d4 = p.d / 4;
     for (int o = tid; o < nvec * d4; o += kDecodeMergeThreads) {
       const int i = o / d4;
       const int dd = (o - i * d4) * 4;
-      const long long orow = s_orow[i];
+      const int qi = q0 + i;
+      const int r = qi / p.group;
+      const int g = qi - r * p.group;
+      const long long orow = (static_cast<long long>(b) * p.rows + r) * p.h_q + static_cast<long long>(h) * p.group + g;
       const float4* acc = reinterpret_cast<const float4*>(p.acc_part + orow * p.max_splits * p.d + dd);
-      const int stride4 = p.d / 4;
       float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < S; s0 += 16) {
-        float4 a[16];
+      for (int s0 = 0; s0 < S; s0 += 32) {
+        float4 a[32];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          a[k] = (s0 + k < S) ? acc[static_cast<long long>(s0 + k) * stride4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 32; ++k)
+          a[k] = (s0 + k < S) ? acc[static_cast<long long>(s0 + k) * d4] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < 32; ++k) {
           if (s0 + k >= S) break;
-          const float w = s_m[i][s0 + k];
+          const float w = s_w[i][s0 + k];
           if (w != -1.f) {
             A.x += w * a[k].x;
             A.y += w * a[k].y;
@@ -282,8 +310,8 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
         }
       }
       const float sc = s_scale[i];
-      float4 r = s_dead[i] ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A.x * sc, A.y * sc, A.z * sc, A.w * sc);
-      *reinterpret_cast<float4*>(p.out + orow * p.d + dd) = r;
+      const float4 res = s_dead[i] ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A.x * sc, A.y * sc, A.z * sc, A.w * sc);
+      *reinterpret_cast<float4*>(p.out + orow * p.d + dd) = res;
     }
     __syncthreads();
   }
