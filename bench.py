@@ -416,7 +416,7 @@ def main():
         "dtype": "f32",
         "data": "synthetic (seeded: workloads/)",
         "config": config_block(case, args),
-        "roofline": {"bound": "hbm", "kernel": "decode (plan_kernel + decode_partial_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "decode call (plan_kernel + decode_partial_kernel + decode_merge_kernel)",
                      "achieved": round(dec_achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_achieved / peak, 4), "frac_of_nominal_8000": round(dec_achieved / 8000.0, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"

@@ -102,7 +102,7 @@ NBX_API int nbx_paged_kv_append(const void* new_k, const void* new_v, int new_dt
 
 /*
  * nbx_paged_decode_workspace_bytes -- bytes of workspace nbx_paged_decode_attn needs for
- * these sizes (the split plan, the work list, the merge tickets and the fp32 split partials).
+ * these sizes (the split plan, the work list and the fp32 split partials).
  * Returns 0 if the sizes are invalid. max_seq_len is the host-known bound on seq_lens.
  */
 NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len);
