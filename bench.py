@@ -244,7 +244,11 @@ def run_gpu(args, rank: int, world: int):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         sess.step(stream=stream)
-    launches_per_step = 3 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 2
+    # our kernels per call: append (when the step has new tokens), plan, partial, and the merge
+    # when some sequence can have more than one split
+    merge = 1 if case.max_seq_len > 256 else 0
+    decode_launches = 2 + merge
+    launches_per_step = decode_launches + (1 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 0)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -306,7 +310,16 @@ def run_gpu(args, rank: int, world: int):
     total_bytes = all_reduce_sum(float(kv_bytes), world)
     return dict(case=case, kv_bytes=kv_bytes, total_bytes=total_bytes, ms_per_step=t_max, dec_ms=dec_max,
                 e2e_ms=e2e_max, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
-                launches=launches_per_step * args.steps + 2 * args.steps, step_ms=step_ms)
+                launches=(launches_per_step + decode_launches) * args.steps, step_ms=step_ms,
+                partial=partial_kernel_name(cfg))
+
+
+def partial_kernel_name(cfg) -> str:
+    import paged_split_kv_append_gb300 as nbx
+    code = {"f32": nbx.NBX_F32, "bf16": nbx.NBX_BF16, "e4m3": nbx.NBX_E4M3}
+    kind = nbx.nbx_paged_decode_partial_kernel(code[cfg.q_dtype], code[cfg.pool_dtype], cfg.rows, cfg.h_q, cfg.h_kv,
+                                               cfg.d, 1, cfg.page_tokens)
+    return "decode_partial_mma_kernel" if kind == nbx.PARTIAL_TCGEN05 else "decode_partial_kernel"
 
 
 def barrier(world: int):
@@ -416,7 +429,7 @@ def main():
         "dtype": "f32",
         "data": "synthetic (seeded: workloads/)",
         "config": config_block(case, args),
-        "roofline": {"bound": "hbm", "kernel": "decode call (plan_kernel + decode_partial_kernel + decode_merge_kernel)",
+        "roofline": {"bound": "hbm", "kernel": f"decode call (plan_kernel + {r['partial']} + decode_merge_kernel)",
                      "achieved": round(dec_achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_achieved / peak, 4), "frac_of_nominal_8000": round(dec_achieved / 8000.0, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"

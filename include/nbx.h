@@ -184,6 +184,28 @@ NBX_API int nbx_paged_decode_attn_noalloc(const void* q, int q_dtype, int batch,
                                           const int32_t* seq_lens, int max_seq_len, float scale, float k_scale,
                                           float v_scale, float* out, int32_t* status, void* stream);
 
+/* The split-partial kernel a decode call runs (see nbx_paged_decode_partial_kernel). */
+typedef enum {
+    NBX_PARTIAL_SIMT = 0,    /* CUDA cores: work units of 4 query vectors, any supported shape */
+    NBX_PARTIAL_TCGEN05 = 1  /* tensor cores (tcgen05.mma): work units of 128 query vectors */
+} nbx_partial_kernel;
+
+/*
+ * nbx_paged_decode_partial_kernel -- which split-partial kernel nbx_paged_decode_attn (and
+ * nbx_paged_decode_attn_noalloc) runs for these sizes and formats. Host-only; launches nothing.
+ * (TensorFold PR #1219: the rows of one KV head read each K/V tile once; when rows x group
+ * reaches a dense tile the QK^T and PV products become matrix products.)
+ *
+ * Returns NBX_PARTIAL_TCGEN05 when rows * (h_q / h_kv) >= 64, q_dtype and pool_dtype are both
+ * NBX_BF16, d is 128 or 256, page_tokens is a multiple of 64 and the pool has fewer than 2^31 - 64
+ * rows of d elements per K or V; NBX_PARTIAL_SIMT for every other supported case; a negative
+ * nbx_status for arguments nbx_paged_decode_attn rejects (shape, page alignment, dtype). Both
+ * kernels compute the same partials to within the decode's tolerance; neither depends on page
+ * ids or on the grid size.
+ */
+NBX_API int nbx_paged_decode_partial_kernel(int q_dtype, int pool_dtype, int rows, int h_q, int h_kv, int d,
+                                            int num_pages, int page_tokens);
+
 /*
  * nbx_set_decode_grid_limit -- cap the number of CTAs nbx_paged_decode_attn launches (0 = the
  * default, two per SM). Process-wide; the output is bit-identical for every value.

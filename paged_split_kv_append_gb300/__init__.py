@@ -29,6 +29,7 @@ __all__ = [
 
 NBX_F32, NBX_BF16, NBX_E4M3 = 0, 1, 2
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+PARTIAL_SIMT, PARTIAL_TCGEN05 = 0, 1
 
 _lib = None
 _lock = threading.Lock()
@@ -64,6 +65,8 @@ def _declare(l):
     l.nbx_paged_decode_attn.restype = i32
     l.nbx_paged_decode_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     l.nbx_paged_decode_merge.restype = i32
+    l.nbx_paged_decode_partial_kernel.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    l.nbx_paged_decode_partial_kernel.restype = i32
     l.nbx_set_decode_grid_limit.argtypes = [i32]
     l.nbx_set_decode_grid_limit.restype = None
     l.nbx_status_string.argtypes = [i32]
@@ -200,6 +203,14 @@ def nbx_paged_decode_merge(acc_part: torch.Tensor, m_part: torch.Tensor, l_part:
                                       _stream(stream))
     _check("nbx_paged_decode_merge", st)
     return out
+
+
+def nbx_paged_decode_partial_kernel(q_dtype: int, pool_dtype: int, rows: int, h_q: int, h_kv: int, d: int,
+                                    num_pages: int, page_tokens: int) -> int:
+    """PARTIAL_SIMT or PARTIAL_TCGEN05: the split-partial kernel a decode with these sizes runs."""
+    k = lib().nbx_paged_decode_partial_kernel(q_dtype, pool_dtype, rows, h_q, h_kv, d, num_pages, page_tokens)
+    _check("nbx_paged_decode_partial_kernel", k if k < 0 else 0)
+    return k
 
 
 def nbx_set_decode_grid_limit(max_ctas: int) -> None:

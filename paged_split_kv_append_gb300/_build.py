@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libnbx.so")
 SOURCES = ["abi.cu", "append.cu", "decode_common.cu", "decode_f32.cu", "decode_bf16.cu", "decode_e4m3.cu",
-           "noalloc.cu"]
+           "decode_mma.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", INCLUDE]

@@ -105,6 +105,23 @@ static bool decode_shape_ok(int batch, int rows, int h_q, int h_kv, int d, int m
   return true;
 }
 
+NBX_API int nbx_paged_decode_partial_kernel(int q_dtype, int pool_dtype, int rows, int h_q, int h_kv, int d,
+                                            int num_pages, int page_tokens) {
+  if (!decode_shape_ok(1, rows, h_q, h_kv, d, 0) || num_pages < 1 || page_tokens < 1) return NBX_ERR_SHAPE;
+  if ((page_tokens % NBX_TILE_POSITIONS) != 0) return NBX_ERR_PAGE_ALIGN;
+  if (q_dtype != NBX_F32 && q_dtype != NBX_BF16) return NBX_ERR_DTYPE;
+  if (pool_dtype != NBX_F32 && pool_dtype != NBX_BF16 && pool_dtype != NBX_E4M3) return NBX_ERR_DTYPE;
+  DecodeParams p = {};
+  p.rows = rows;
+  p.h_q = h_q;
+  p.h_kv = h_kv;
+  p.group = h_q / h_kv;
+  p.d = d;
+  p.num_pages = num_pages;
+  p.page_tokens = page_tokens;
+  return mma_path_applies(p, q_dtype, pool_dtype) ? NBX_PARTIAL_TCGEN05 : NBX_PARTIAL_SIMT;
+}
+
 NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len) {
   if (!decode_shape_ok(batch, rows, h_q, h_kv, d, max_seq_len)) return 0;
   WorkspaceLayout w;

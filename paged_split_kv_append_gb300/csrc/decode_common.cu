@@ -322,7 +322,8 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (pool_dtype == NBX_F32) e = decode_dispatch_F32(p, q_dtype, grid_limit, stream);
+  if (mma_path_applies(p, q_dtype, pool_dtype)) e = decode_dispatch_mma(p, grid_limit, stream);
+  else if (pool_dtype == NBX_F32) e = decode_dispatch_F32(p, q_dtype, grid_limit, stream);
   else if (pool_dtype == NBX_BF16) e = decode_dispatch_BF16(p, q_dtype, grid_limit, stream);
   else e = decode_dispatch_E4M3(p, q_dtype, grid_limit, stream);
   if (e != cudaSuccess) return e;

@@ -94,6 +94,12 @@ struct DecodeParams {
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);
 
+// The tensor-core partial kernel: used when the query vectors of one KV head fill an MMA tile
+// (rows x group >= 64), q and pools are bf16, d is 128 or 256 and pages hold a multiple of 64
+// positions.
+bool mma_path_applies(const DecodeParams& p, int q_dtype, int pool_dtype);
+cudaError_t decode_dispatch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream);
+
 // Launch with programmatic dependent launch: the grid may start while the previous kernel in the
 // stream finishes; the kernel orders itself after it with griddepcontrol.wait.
 template <typename... KArgs, typename... Args>

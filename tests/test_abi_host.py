@@ -125,3 +125,23 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(nbx._build, "LIB", str(tmp_path / "missing" / "libnbx.so"))
     with pytest.raises(nbx.NbxLibraryMissing):
         nbx.lib()
+
+
+def test_partial_kernel_choice(lib):
+    # rows x group >= 64 with bf16 q and pools, d 128/256, 64-position pages: tensor cores
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 256, 1000, 64) == \
+        nbx.PARTIAL_TCGEN05                                   # verify window: 16 rows x 6 heads
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 8, 32, 4, 128, 1000, 128) == \
+        nbx.PARTIAL_TCGEN05                                   # exactly 64 query vectors
+    simt = [(nbx.NBX_BF16, nbx.NBX_BF16, 1, 32, 8, 128, 1000, 16),     # single-row decode
+            (nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 256, 1000, 16),    # pages of 16 positions
+            (nbx.NBX_F32, nbx.NBX_BF16, 16, 24, 4, 256, 1000, 64),     # fp32 queries
+            (nbx.NBX_BF16, nbx.NBX_F32, 16, 24, 4, 256, 1000, 64),     # fp32 pool
+            (nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 64, 1000, 64),     # d = 64
+            (nbx.NBX_BF16, nbx.NBX_BF16, 7, 36, 4, 128, 1000, 64),     # 63 query vectors
+            (nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 256, 2 ** 23, 64)]  # pool rows beyond 2^31 - 64
+    for args in simt:
+        assert nbx.nbx_paged_decode_partial_kernel(*args) == nbx.PARTIAL_SIMT, args
+    assert lib.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 5, 256, 10, 64) == -2
+    assert lib.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 256, 10, 40) == -4
+    assert lib.nbx_paged_decode_partial_kernel(7, nbx.NBX_BF16, 16, 24, 4, 256, 10, 64) == -3

@@ -1,0 +1,111 @@
+"""GPU parity of the tensor-core split partial (tcgen05) against the float64 oracle.
+
+The decode runs this kernel when the query vectors of one KV head fill an MMA tile
+(rows x group >= 64, bf16 q and pools, d 128 or 256, pages of a multiple of 64 positions):
+multi-row verify windows and prefill chunks. Same bars as the SIMT kernel: max |err| 2e-3 for
+bf16 pools, bit-identical under page relabelling, grid size and batch order; pools start as NaN.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle.paged as op
+import paged_split_kv_append_gb300 as nbx
+import workloads as wl
+from tests import pins
+from tests.test_gpu_parity import DEV, check_against_oracle, run_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    nbx.build()
+    nbx.nbx_set_decode_grid_limit(0)
+    yield
+    nbx.nbx_set_decode_grid_limit(0)
+
+
+def tc_config(name, batch, rows, h_q, h_kv, d, page, lens, seed):
+    cfg = wl.Config(name, batch, rows, h_q, h_kv, d, page, "bf16", "bf16", seed, lens)
+    kind = nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, rows, h_q, h_kv, d, 1000, page)
+    assert kind == nbx.PARTIAL_TCGEN05, cfg
+    return cfg
+
+
+# lengths around the 64-position tile, the 256-position split grain and the page; 0 and
+# lengths below the window (rows that see no key)
+EDGE_LENS = (0, 1, 15, 16, 17, 63, 64, 65, 257, 511, 512, 513, 4097)
+
+
+def test_verify_window_edge_lengths():
+    cfg = tc_config("tc_edges", len(EDGE_LENS), 16, 24, 4, 256, 64, ("fixed", EDGE_LENS), 31)
+    case = wl.make_case(cfg, device=DEV)
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+    o = out.cpu().numpy()
+    assert np.all(o[0] == 0.0)                     # empty sequence
+    assert np.all(o[1, :15] == 0.0)                # length 1: rows 0..14 see no key
+
+
+def test_head_dim_128_with_exactly_one_half_tile():
+    # 8 rows x group 8 = 64 query vectors: half of the 128-lane tile is padding
+    cfg = tc_config("tc_d128", 4, 8, 32, 4, 128, 64, ("uniform", 1, 3000), 32)
+    case = wl.make_case(cfg, device=DEV)
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+
+
+def test_several_query_tiles_per_head():
+    # 32 rows x group 6 = 192 query vectors: two M tiles per (split, KV head), pages of 128
+    cfg = tc_config("tc_mtiles", 2, 32, 24, 4, 256, 128, ("uniform", 20, 2000), 33)
+    case = wl.make_case(cfg, device=DEV)
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+
+
+def test_page_permutation_is_bit_exact():
+    case = wl.make_case("verify_small", device=DEV)
+    _, out_a = run_step(case)
+    _, bt2 = wl.permute_pages(case, seed=5)
+    case2 = wl.Case(**{**case.__dict__, "block_table": bt2})
+    _, out_b = run_step(case2)
+    assert torch.equal(out_a, out_b)
+
+
+def test_grid_limits_with_several_query_tiles_are_bit_exact():
+    cfg = tc_config("tc_mtiles_grid", 2, 32, 24, 4, 256, 64, ("fixed", (1500, 700)), 34)
+    case = wl.make_case(cfg, device=DEV)
+    _, ref = run_step(case)
+    for limit in (1, 5, 151, 4000):
+        _, out = run_step(case, grid_limit=limit)
+        assert torch.equal(out, ref), f"grid limit {limit}"
+
+
+def test_nan_key_reaches_only_its_heads():
+    case = wl.make_case("verify_small", device=DEV, lens=[1000, 300])
+    case.k_raw[int(case.tok_offset[0]) + 700, 0, 9] = float("nan")
+    _, out = run_step(case)
+    o = out.cpu().numpy()
+    G = case.cfg.group
+    assert np.all(np.isnan(o[0, :, :G]))           # every row of sequence 0 sees position 700
+    assert np.all(np.isfinite(o[0, :, G:])) and np.all(np.isfinite(o[1]))
+
+
+def test_missing_page_sets_status_and_spares_other_sequences():
+    case = wl.make_case("verify_small", device=DEV, lens=[900, 1300])
+    sess = bench.session_for_case(case, DEV)
+    bt = sess.block_table.clone()
+    bt[1, 2] = -1
+    bt[1, 4] = case.num_pages + 3
+    sess.block_table = bt
+    out = sess.step()
+    torch.cuda.synchronize()
+    assert sess.status_bits() & nbx.DEV_BAD_PAGE
+    kp, vp = pins.oracle_pools(case)
+    ref = op.decode_attention(case.q.float().cpu().numpy()[:1], kp, vp, "bf16", case.block_table[:1], case.lens[:1],
+                              case.cfg.page_tokens, case.scale)
+    assert np.max(np.abs(out.cpu().numpy()[:1] - ref)) <= 2e-3
+    assert np.all(np.isfinite(out.cpu().numpy()[1]))   # the missing pages' positions are skipped
