@@ -46,14 +46,16 @@ KERNEL_SOURCES = ("paged_split_kv_append_gb300/csrc/decode_kernels.cuh",
 
 
 # ------------------------------------------------------------------------------------------ shared set-up
-def session_for_case(case: "wl.Case", device, fill_nan: bool = True, prefill: bool = True):
+def session_for_case(case: "wl.Case", device, fill_nan: bool = True, prefill: bool = True, widen: bool = True):
     """The device state of one workload: pools prefilled through nbx_paged_kv_append with every
-    position but the step's, and the step's inputs (queries, tables, lengths, new tokens)."""
+    position but the step's, and the step's inputs (queries, tables, lengths, new tokens).
+    widen=False sizes the workspace without room for the bf16 copies of an fp8 pool."""
     from paged_split_kv_append_gb300.session import PagedDecodeSession
     cfg = case.cfg
     sess = PagedDecodeSession(num_pages=case.num_pages, h_kv=cfg.h_kv, page_tokens=cfg.page_tokens, d=cfg.d,
                               pool_dtype=cfg.pool_dtype, batch=cfg.batch, rows=cfg.rows, h_q=cfg.h_q,
-                              max_seq_len=case.max_seq_len, device=device, fill_nan=fill_nan)
+                              max_seq_len=case.max_seq_len, device=device, fill_nan=fill_nan,
+                              q_dtype=cfg.q_dtype, widen=widen)
     sess.k_scale, sess.v_scale = case.k_scale, case.v_scale
     if prefill:
         idx, slots = case.prefill_index()
@@ -247,7 +249,8 @@ def run_gpu(args, rank: int, world: int):
     # our kernels per call: append (when the step has new tokens), plan, partial, and the merge
     # when some sequence can have more than one split
     merge = 1 if case.max_seq_len > 256 else 0
-    decode_launches = 2 + merge
+    widen = 1 if partial_kernel_name(cfg).startswith("widen") else 0
+    decode_launches = 2 + merge + widen
     launches_per_step = decode_launches + (1 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 0)
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -319,6 +322,8 @@ def partial_kernel_name(cfg) -> str:
     code = {"f32": nbx.NBX_F32, "bf16": nbx.NBX_BF16, "e4m3": nbx.NBX_E4M3}
     kind = nbx.nbx_paged_decode_partial_kernel(code[cfg.q_dtype], code[cfg.pool_dtype], cfg.rows, cfg.h_q, cfg.h_kv,
                                                cfg.d, 1, cfg.page_tokens)
+    if kind == nbx.PARTIAL_TCGEN05_WIDENED:
+        return "widen_kernel + decode_partial_mma_kernel"
     return "decode_partial_mma_kernel" if kind == nbx.PARTIAL_TCGEN05 else "decode_partial_kernel"
 
 

@@ -108,6 +108,17 @@ NBX_API int nbx_paged_kv_append(const void* new_k, const void* new_v, int new_dt
 NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len);
 
 /*
+ * nbx_paged_decode_workspace_bytes_for -- the workspace for these sizes and formats, with room for
+ * the bf16 copies an fp8 (NBX_E4M3) pool needs to run on tensor cores when the call qualifies
+ * (nbx_paged_decode_partial_kernel returns NBX_PARTIAL_TCGEN05_WIDENED): 2 x batch x
+ * ceil(max_seq_len / 64) x 64 x h_kv x d x 2 bytes more. This library addition has no counterpart in
+ * the method's pages. For every other case it equals nbx_paged_decode_workspace_bytes. Returns 0
+ * if the sizes are invalid.
+ */
+NBX_API size_t nbx_paged_decode_workspace_bytes_for(int q_dtype, int pool_dtype, int batch, int rows, int h_q,
+                                                    int h_kv, int d, int max_seq_len, int page_tokens);
+
+/*
  * nbx_paged_decode_attn -- split-KV decode attention read through the block table.
  * (nbxtensor/ops/attention_wrappers.py, paged_decode_attention; nbxtensor/ops/paged_decode_attn.py,
  * paged_decode_splits and paged_decode_attn_split_kernel; TensorFold PR #1219, rows-first grid.)
@@ -130,7 +141,9 @@ NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, in
  *   scale        softmax scale (finite); k_scale, v_scale: pool scales (finite, > 0)
  *   out          [device] fp32 [batch, rows, h_q, d]
  *   workspace    [device] at least nbx_paged_decode_workspace_bytes(...) bytes, 256-byte aligned;
- *                its contents need no initialisation and are overwritten
+ *                its contents need no initialisation and are overwritten. With an fp8 pool and a
+ *                workspace of nbx_paged_decode_workspace_bytes_for(...) bytes, a multi-row window runs
+ *                on tensor cores over exact bf16 copies of its K/V made in the workspace
  *   status       [device] int32 or NULL
  *   stream       cudaStream_t
  * Requirements: h_q % h_kv == 0; d in {64, 128, 256}; page_tokens a multiple of
@@ -186,8 +199,11 @@ NBX_API int nbx_paged_decode_attn_noalloc(const void* q, int q_dtype, int batch,
 
 /* The split-partial kernel a decode call runs (see nbx_paged_decode_partial_kernel). */
 typedef enum {
-    NBX_PARTIAL_SIMT = 0,    /* CUDA cores: work units of 4 query vectors, any supported shape */
-    NBX_PARTIAL_TCGEN05 = 1  /* tensor cores (tcgen05.mma): work units of 128 query vectors */
+    NBX_PARTIAL_SIMT = 0,            /* CUDA cores: work units of 4 query vectors, any supported shape */
+    NBX_PARTIAL_TCGEN05 = 1,         /* tensor cores (tcgen05.mma): work units of 128 query vectors */
+    NBX_PARTIAL_TCGEN05_WIDENED = 2  /* fp8 pool: the tensor-core kernel on bf16 copies of the sequences'
+                                        K/V in the workspace, when the call's workspace holds them
+                                        (nbx_paged_decode_workspace_bytes_for); otherwise SIMT */
 } nbx_partial_kernel;
 
 /*
@@ -196,9 +212,10 @@ typedef enum {
  * (TensorFold PR #1219: the rows of one KV head read each K/V tile once; when rows x group
  * reaches a dense tile the QK^T and PV products become matrix products.)
  *
- * Returns NBX_PARTIAL_TCGEN05 when rows * (h_q / h_kv) >= 64, q_dtype and pool_dtype are both
- * NBX_BF16, d is 128 or 256, page_tokens is a multiple of 64 and the pool has fewer than 2^31 - 64
- * rows of d elements per K or V; NBX_PARTIAL_SIMT for every other supported case; a negative
+ * Returns NBX_PARTIAL_TCGEN05 when rows * (h_q / h_kv) >= 64, h_q / h_kv <= 128, q_dtype and
+ * pool_dtype are both NBX_BF16, d is 128 or 256, page_tokens is a multiple of 64 and the pool has
+ * fewer than 2^31 - 64 rows of d elements per K or V (the call itself also needs scale > 0; a
+ * decode with scale <= 0 runs the SIMT kernel); NBX_PARTIAL_SIMT for every other supported case; a negative
  * nbx_status for arguments nbx_paged_decode_attn rejects (shape, page alignment, dtype). Both
  * kernels compute the same partials to within the decode's tolerance; neither depends on page
  * ids or on the grid size.

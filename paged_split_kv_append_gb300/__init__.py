@@ -29,7 +29,7 @@ __all__ = [
 
 NBX_F32, NBX_BF16, NBX_E4M3 = 0, 1, 2
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
-PARTIAL_SIMT, PARTIAL_TCGEN05 = 0, 1
+PARTIAL_SIMT, PARTIAL_TCGEN05, PARTIAL_TCGEN05_WIDENED = 0, 1, 2
 
 _lib = None
 _lock = threading.Lock()
@@ -60,6 +60,8 @@ def _declare(l):
     l.nbx_paged_kv_append.restype = i32
     l.nbx_paged_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     l.nbx_paged_decode_workspace_bytes.restype = sz
+    l.nbx_paged_decode_workspace_bytes_for.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32]
+    l.nbx_paged_decode_workspace_bytes_for.restype = sz
     l.nbx_paged_decode_attn.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp, i32, vp, i32,
                                         f32, f32, f32, vp, vp, sz, vp, vp]
     l.nbx_paged_decode_attn.restype = i32
@@ -153,6 +155,12 @@ def nbx_paged_decode_workspace_bytes(batch: int, rows: int, h_q: int, h_kv: int,
     return int(lib().nbx_paged_decode_workspace_bytes(batch, rows, h_q, h_kv, d, max_seq_len))
 
 
+def nbx_paged_decode_workspace_bytes_for(q_dtype: int, pool_dtype: int, batch: int, rows: int, h_q: int, h_kv: int,
+                                         d: int, max_seq_len: int, page_tokens: int) -> int:
+    return int(lib().nbx_paged_decode_workspace_bytes_for(q_dtype, pool_dtype, batch, rows, h_q, h_kv, d,
+                                                          max_seq_len, page_tokens))
+
+
 def nbx_paged_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
                           seq_lens: torch.Tensor, max_seq_len: int, scale: float, k_scale: float = 1.0,
                           v_scale: float = 1.0, out: Optional[torch.Tensor] = None,
@@ -176,7 +184,8 @@ def nbx_paged_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
     if out is None:
         out = torch.empty((batch, rows, h_q, d), dtype=torch.float32, device=q.device)
     _cuda_contig("out", out)
-    need = nbx_paged_decode_workspace_bytes(batch, rows, h_q, h_kv, d, max_seq_len)
+    need = nbx_paged_decode_workspace_bytes_for(dtype_code(q), dtype_code(k_pool), batch, rows, h_q, h_kv, d,
+                                                max_seq_len, page_tokens)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     st = lib().nbx_paged_decode_attn(_ptr(q), dtype_code(q), batch, rows, h_q, d, _ptr(k_pool), _ptr(v_pool),

@@ -13,7 +13,8 @@ int splits_for(int length) {
   return s < 1 ? 1 : (s > NBX_MAX_SPLITS ? NBX_MAX_SPLITS : s);
 }
 
-bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* w) {
+bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* w,
+                      bool widen) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t S = static_cast<size_t>(splits_for(max_seq_len));
   const size_t rb = (static_cast<size_t>(rows) * (h_q / h_kv) + kQB - 1) / kQB;
@@ -32,6 +33,20 @@ bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq
   off += up(prow * 4);
   w->acc_part = off;
   off += up(prow * static_cast<size_t>(d) * 4);
+  w->t64 = 0;
+  w->widen_k = w->widen_v = w->widen_bt = off;
+  if (widen) {
+    const size_t t64 = (static_cast<size_t>(max_seq_len < 1 ? 1 : max_seq_len) + 63) / 64;
+    const size_t bytes = static_cast<size_t>(batch) * t64 * h_kv * 64 * d * 2;
+    if (static_cast<size_t>(batch) * t64 * h_kv * 64 >= (static_cast<size_t>(1) << 31) - 64) return false;
+    w->t64 = static_cast<int>(t64);
+    w->widen_k = off;
+    off += up(bytes);
+    w->widen_v = off;
+    off += up(bytes);
+    w->widen_bt = off;
+    off += up(static_cast<size_t>(batch) * t64 * 4);
+  }
   w->total = off;
   w->max_splits = static_cast<int>(S);
   w->row_blocks = static_cast<int>(rb);
@@ -107,6 +122,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
           e.s = s;
           e.start = s * sp.seg;
           e.end = min((s + 1) * sp.seg, sp.len);
+          e.len = sp.len;
+          e.n_splits = sp.n_splits;
+          e.pad0 = e.pad1 = 0;
           p.entries[base + s] = e;
         }
         base += sp.n_splits;
@@ -169,6 +187,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
     en.s = s;
     en.start = s * s_seg[b];
     en.end = min((s + 1) * s_seg[b], s_len[b]);
+    en.len = s_len[b];
+    en.n_splits = s_n[b];
+    en.pad0 = en.pad1 = 0;
     p.entries[e] = en;
   }
   if (tid == 0) p.header[0] = total;
@@ -322,7 +343,8 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (mma_path_applies(p, q_dtype, pool_dtype)) e = decode_dispatch_mma(p, grid_limit, stream);
+  if (p.widen_k != nullptr) e = decode_dispatch_widened(p, grid_limit, stream);
+  else if (mma_path_applies(p, q_dtype, pool_dtype)) e = decode_dispatch_mma(p, grid_limit, stream);
   else if (pool_dtype == NBX_F32) e = decode_dispatch_F32(p, q_dtype, grid_limit, stream);
   else if (pool_dtype == NBX_BF16) e = decode_dispatch_BF16(p, q_dtype, grid_limit, stream);
   else e = decode_dispatch_E4M3(p, q_dtype, grid_limit, stream);

@@ -8,29 +8,36 @@
 // nbxtensor/ops/attention_wrappers.py, _math_attention, and as TensorFold PR #1219 ("Gotchas")
 // describes for its attn_rows kernel: each K/V tile is read once for all rows of a stream.
 //
-// GB300 design (one CTA per SM, 6 warps):
+// GB300 design (one CTA per SM, 7 warps):
 //  * Work unit = (split entry, KV head, M tile), M tile fastest. An M tile holds Rt whole query
-//    rows x the G query heads of the KV head (Rt = min(rows, 128 / G)), so its Q block, its output
-//    block and its partial block are boxes of 4-D / 5-D tensor maps. Static round-robin over the
-//    plan's longest-first list.
-//  * warp 4 (producer, one thread): an event loop over three TMA streams -- the unit's Q box, K
-//    tiles and V tiles of 64 positions (a page, or a 64-aligned part of one) into separate rings,
-//    128-byte swizzle -- issuing whichever has a free slot. A page id outside the pool loads rows
-//    before the tensor, which read as zeros, and its positions are masked.
-//  * warp 5 (MMA): holds the TMEM; an event loop issues, as soon as their inputs are ready,
-//      S[x % 2] = Q K(x)^T                    M=128, N=64, K=d; A, B from shared memory
-//      O       += P_hi(y) V(y) + P_lo(y) V(y)  M=128, N=d, K=64; P from TMEM, V MN-major
-//    (kind::f16, bf16 x bf16 -> fp32 in TMEM) and signals completions with tcgen05.commit. P
-//    enters the product as two bf16 terms, P_hi = bf16(p) and P_lo = bf16(p - P_hi), so the
-//    weights keep about 16 bits. The warp zeroes V rows past a split's end before their PV
-//    (0 x NaN would otherwise leak) and skips 16-position steps that hold none.
+//    rows x the G query heads of the KV head (Rt = min(rows, 128 / G)), so its Q block is a box
+//    of a 4-D tensor map. Static round-robin over the plan's longest-first list; the next unit's
+//    work-list entry is loaded one unit ahead.
+//  * Shared memory: the unit's Q tile (128-byte-swizzled K-major atoms of 64 columns), a K ring and
+//    a V ring of 16 KB slots (64 positions x 128 columns: half of a d=256 tile, a whole d=128
+//    tile; a tile is one page or a 64-aligned part of one), and per-warp epilogue staging. Every
+//    slot has a full barrier (TMA bytes) and an empty barrier (its consumer).
+//  * warps 4 and 6 (producers) fill the K ring and the V ring with TMA (cp.async.bulk.tensor),
+//    one thread issuing while the warp's lanes fetch block-table ids a chunk ahead. A page id
+//    outside the pool loads rows before the tensor, which read as zeros; its positions are
+//    masked. K halves free their slots at QK^T and V halves at PV, so the K stream runs ahead.
+//  * TMEM (512 columns): three S/P buffers [0, 192), O [192, 192 + d). Three buffers let QK^T run
+//    two tiles ahead of PV, which hides the completion latency of the tcgen05.commit hand-offs.
+//  * warp 5 (MMA) holds the TMEM; an event loop issues, as soon as their inputs are ready,
+//      S[x % 3] = Q K(x)^T                    M=128, N=64, K=d; Q and K from shared memory
+//      O       += P_hi(y) V(y) + P_lo(y) V(y)  M=128, N=128 per V half, K=64; P from TMEM
+//    (kind::f16, bf16 x bf16 -> fp32 in TMEM), loads the next unit's Q tile by TMA once the
+//    current unit's last QK^T has completed, and signals completions with tcgen05.commit. P
+//    enters the product as two bf16 terms, P_hi = p truncated to bf16 and P_lo = (p - P_hi)
+//    truncated, so the weights keep 15 bits or more. The warp zeroes V rows past a split's end
+//    before their PV (0 x NaN would otherwise leak) and skips 16-position steps that hold none.
 //  * warps 0-3 (softmax, one query vector per thread = one TMEM lane): read S from TMEM, mask
 //    (split end, causal row position, missing pages), run the online softmax in log2 units with
 //    the lazy rescale (O is rescaled in TMEM only when a row's max grows by more than 2^8), and
-//    write P_hi / P_lo over the S columns they came from. At the end of a unit they move O from
-//    TMEM through 128-byte-swizzled shared memory to TMA tensor stores: the partial, or the
-//    normalised output when the sequence has one split. Rows past the sequence's last row are
-//    outside the tensor's row dimension, so the stores leave them alone.
+//    write P_hi / P_lo over the S columns they came from. After the unit's last PV they store O:
+//    each warp moves its 32 TMEM lanes through its own swizzled staging rows in shared memory to
+//    coalesced 128-byte row segments -- the partial, or the normalised output when the sequence
+//    has one split.
 //  * Every wait is bounded. On timeout the kernel records NBX_DEV_TIMEOUT, waits (bounded) for
 //    its copies and MMAs in flight, releases its TMEM and returns.
 #include <atomic>
@@ -45,33 +52,37 @@ namespace {
 
 constexpr int kMmaM = 128;       // TMEM lanes / rows of an M tile
 constexpr int kMmaN = 64;        // positions per K/V tile
-constexpr int kMmaThreads = 192;
+constexpr int kMmaThreads = 224;
 constexpr int kSoftmaxThreads = 128;
 constexpr float kMmaTau = 8.0f;  // lazy-rescale threshold, log2 units
-constexpr int kChunk = 32;       // output columns per epilogue store
+constexpr int kChunk = 32;       // output columns per epilogue step
+constexpr int kSBufs = 3;        // S/P buffers in TMEM
+constexpr int kSlotBytes = 16384;  // ring slot: 64 positions x 128 columns bf16
 
 template <int D>
 struct MmaCfg {
-  static constexpr int kStages = D <= 128 ? 4 : 2;    // K slots, and as many V slots
-  static constexpr int kQBytes = kMmaM * D * 2;
-  static constexpr int kTileBytes = kMmaN * D * 2;     // one K or V tile, bf16
-  static constexpr int kStgBytes = kMmaM * kChunk * 4;  // one epilogue staging buffer
+  static constexpr int kHalves = D / 128;                  // ring slots per K (or V) tile
+  static constexpr int kKSlots = D <= 128 ? 5 : 4;         // K ring
+  static constexpr int kVSlots = kKSlots;                  // V ring
+  static constexpr int kQBytes = kMmaM * D * 2;            // Q tile, D / 64 atoms of 16 KB
+  static constexpr int kStgBytes = 4 * 2 * 32 * kChunk * 4;  // epilogue: 4 warps x 2 buffers x 32 rows
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kStgOff = kVOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kStgOff + 2 * kStgBytes;
+  static constexpr int kVOff = kKOff + kKSlots * kSlotBytes;
+  static constexpr int kStgOff = kVOff + kVSlots * kSlotBytes;
+  static constexpr int kBarOff = kStgOff + kStgBytes;
   static constexpr int kSmem = kBarOff + 512 + 1024;   // barriers + slack for 1024-byte alignment
-  static constexpr uint32_t kTmemCols = D <= 128 ? 256 : 512;
-  static constexpr uint32_t kOCol = 128;               // S/P buffers at columns 0 and 64, O from 128
+  // TMEM columns: S/P buffers [0, 192), O [192, 192 + D)
+  static constexpr uint32_t kOCol = kSBufs * kMmaN;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kOCol + D <= kTmemCols, "TMEM");
   static_assert(kSmem <= 227 * 1024, "shared memory");
+  static_assert((2 * (kKSlots + kVSlots) + 3 * kSBufs + 6) * 8 <= 512, "barrier area");
 };
 
 struct MmaMaps {
   CUtensorMap k, v;   // 2-D pool views [num_pages * h_kv * page_tokens][d], box 64 x 64
   CUtensorMap q;      // 4-D [batch][rows][h_q][d] bf16, box {64, G, Rt, 1}
-  CUtensorMap out;    // 4-D [batch][rows][h_q][d] fp32, box {32, G, Rt, 1}
-  CUtensorMap part;   // 5-D [batch][rows][h_q][max_splits][d] fp32, box {32, 1, G, Rt, 1}
 };
 
 // ---- tcgen05 / TMA wrappers (inline PTX)
@@ -153,28 +164,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2, int c3) {
-  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
-}
-__device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, const void* src, int c0, int c1, int c2, int c3,
-                                             int c4) {
-  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// every bulk store group but the newest `N` has finished reading shared memory
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// every bulk store group has completed
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Non-blocking test of an mbarrier phase.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -229,113 +218,169 @@ struct MmaUnit {
   int b, s, h, mt, start, end, len, n_splits, tiles;
 };
 
-__device__ __forceinline__ MmaUnit mma_unit(const DecodeParams& p, int u, int m_tiles) {
+__device__ __forceinline__ MmaUnit unit_from(const Entry& en, int u, int span, int m_tiles) {
   MmaUnit m;
-  const int span = p.h_kv * m_tiles;
-  const int e = u / span;
-  const int rem = u - e * span;
+  const int rem = u - (u / span) * span;
   m.h = rem / m_tiles;
   m.mt = rem - m.h * m_tiles;
-  const Entry en = p.entries[e];
   m.b = en.b;
   m.s = en.s;
   m.start = en.start;
   m.end = en.end;
-  const SeqPlan sp = p.plan[en.b];
-  m.len = sp.len;
-  m.n_splits = sp.n_splits;
+  m.len = en.len;
+  m.n_splits = en.n_splits;
   m.tiles = (en.end - en.start + kMmaN - 1) / kMmaN;
   return m;
 }
 
 // Walks this CTA's tiles in order: units blockIdx.x, blockIdx.x + gridDim.x, ..., tiles of each.
+// Ring ordinals: tile tt of the current unit fills slots kbase + tt * hh .. + hh - 1 of the K ring
+// (and the same ordinals of the V ring). The next unit's work-list entry is loaded one unit ahead.
 struct TileIter {
-  int u;        // unit index
-  uint32_t k;   // unit ordinal within this CTA
-  int t;        // tile within the unit
-  uint32_t x;   // tile ordinal within this CTA
+  int u;             // unit index
+  uint32_t k;        // unit ordinal within this CTA
+  int t;             // tile within the unit
+  uint32_t x;        // tile ordinal within this CTA
   bool done;
+  bool has_next;     // another unit follows in this CTA
+  int span;          // units per work-list entry
+  int m_tiles, n_units, hh;
+  uint32_t kbase;
   MmaUnit mu;
-  __device__ __forceinline__ void begin(const DecodeParams& p, int m_tiles, int n_units) {
+  Entry nx;
+  __device__ __forceinline__ void prefetch(const DecodeParams& p) {
+    const int u2 = u + static_cast<int>(gridDim.x);
+    has_next = u2 < n_units;
+    if (has_next) nx = p.entries[u2 / span];
+  }
+  __device__ __forceinline__ void begin(const DecodeParams& p, int m_tiles_, int n_units_, int hh_) {
+    m_tiles = m_tiles_;
+    n_units = n_units_;
+    hh = hh_;
+    span = p.h_kv * m_tiles;
     u = blockIdx.x;
     k = 0;
     t = 0;
     x = 0;
+    kbase = 0;
+    has_next = false;
     done = u >= n_units;
-    if (!done) mu = mma_unit(p, u, m_tiles);
+    if (!done) {
+      mu = unit_from(p.entries[u / span], u, span, m_tiles);
+      prefetch(p);
+    }
   }
-  __device__ __forceinline__ void next_unit(const DecodeParams& p, int m_tiles, int n_units) {
+  __device__ __forceinline__ uint32_t item(int tt) const { return kbase + tt * hh; }
+  __device__ __forceinline__ MmaUnit next_mu() const {
+    return unit_from(nx, u + static_cast<int>(gridDim.x), span, m_tiles);
+  }
+  __device__ __forceinline__ void next_unit(const DecodeParams& p) {
+    kbase += mu.tiles * hh;
     t = 0;
     ++k;
     u += gridDim.x;
     done = u >= n_units;
-    if (!done) mu = mma_unit(p, u, m_tiles);
+    if (!done) {
+      mu = unit_from(nx, u, span, m_tiles);
+      prefetch(p);
+    }
   }
-  __device__ __forceinline__ void next_tile(const DecodeParams& p, int m_tiles, int n_units) {
+  __device__ __forceinline__ void next_tile(const DecodeParams& p) {
     ++x;
-    if (++t >= mu.tiles) next_unit(p, m_tiles, n_units);
+    if (++t >= mu.tiles) next_unit(p);
   }
 };
 
-// First pool row of the tile starting at position n0 of the unit's sequence, or -kMmaN (rows
-// before the tensor, read as zeros) if its page id is outside the pool.
-__device__ __forceinline__ int tile_row(const DecodeParams& p, const MmaUnit& mu, int n0) {
-  const int page = p.block_table[static_cast<int64_t>(mu.b) * p.max_pages + n0 / p.page_tokens];
+// Page id of tile 32 * chunk + lane of a unit (0 past the unit's last tile): one warp fetches the
+// block table 32 tiles at a time.
+__device__ __forceinline__ int chunk_pages(const DecodeParams& p, const MmaUnit& mu, int chunk, int lane) {
+  const int t = chunk * 32 + lane;
+  return t < mu.tiles ? p.block_table[static_cast<int64_t>(mu.b) * p.max_pages + (mu.start + t * kMmaN) / p.page_tokens]
+                      : 0;
+}
+
+// First pool row of the tile at position n0 in page `page`, or -kMmaN (rows before the tensor,
+// read as zeros) if the page id is outside the pool.
+__device__ __forceinline__ int tile_row(const DecodeParams& p, const MmaUnit& mu, int n0, int page, bool report) {
   if (page < 0 || page >= p.num_pages) {
-    raise_status(p.status, NBX_DEV_BAD_PAGE);
+    if (report) raise_status(p.status, NBX_DEV_BAD_PAGE);
     return -kMmaN;
   }
   return (page * p.h_kv + mu.h) * p.page_tokens + (n0 % p.page_tokens);
 }
 
+// Block-table ids of one warp's tile stream: lane l holds the page of tile 32c + l of the current
+// chunk, and the following chunk is loaded one chunk ahead (of this unit, or the next unit's
+// first), so no page-id load sits between two copies.
+struct PageStream {
+  int cur, nxt;
+  __device__ __forceinline__ static int following(const DecodeParams& p, const TileIter& it, int c, int lane) {
+    if ((c + 1) * 32 < it.mu.tiles) return chunk_pages(p, it.mu, c + 1, lane);
+    return it.has_next ? chunk_pages(p, it.next_mu(), 0, lane) : 0;
+  }
+  __device__ __forceinline__ void start(const DecodeParams& p, const TileIter& it, int lane) {
+    cur = chunk_pages(p, it.mu, 0, lane);
+    nxt = following(p, it, 0, lane);
+  }
+  // the iterator has just moved onto a tile t with t % 32 == 0 (a new unit's first tile included)
+  __device__ __forceinline__ void advance(const DecodeParams& p, const TileIter& it, int lane) {
+    cur = nxt;
+    nxt = following(p, it, it.t >> 5, lane);
+  }
+  __device__ __forceinline__ int page(int t) const { return __shfl_sync(0xffffffffu, cur, t & 31); }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     decode_partial_mma_kernel(DecodeParams p, const __grid_constant__ MmaMaps maps) {
   using C = MmaCfg<D>;
-  constexpr int NS = C::kStages;
+  constexpr int NK = C::kKSlots;
+  constexpr int NV = C::kVSlots;
+  constexpr int HI = C::kHalves;
+  constexpr int QA = D / 64;            // Q atoms
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   char* q_s = smem + C::kQOff;
-  char* k_s = smem + C::kKOff;
-  char* v_s = smem + C::kVOff;
+  char* kring = smem + C::kKOff;
+  char* vring = smem + C::kVOff;
   char* stg_s = smem + C::kStgOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
-  uint64_t* k_full = bars;             // [NS]  K tile landed (TMA bytes)
-  uint64_t* k_empty = bars + NS;       // [NS]  QK^T of the slot's tile done
-  uint64_t* v_full = bars + 2 * NS;    // [NS]  V tile landed
-  uint64_t* v_empty = bars + 3 * NS;   // [NS]  PV of the slot's tile done
-  uint64_t* s_full = bars + 4 * NS;    // [2]   S of the buffer's tile in TMEM
-  uint64_t* p_full = s_full + 2;       // [2]   P of the buffer's tile in TMEM (128 arrivals)
-  uint64_t* sp_free = s_full + 4;      // [2]   PV of the buffer's tile done: S/P buffer reusable, O
+  uint64_t* kfull = bars;              // [NK]  the K slot's half landed (TMA bytes)
+  uint64_t* kempty = kfull + NK;       // [NK]  the K slot's half consumed (its QK^T done)
+  uint64_t* vfull = kempty + NK;       // [NV]  the V slot's half landed
+  uint64_t* vempty = vfull + NV;       // [NV]  the V slot's half consumed (its PV done)
+  uint64_t* s_full = vempty + NV;      // [3]   S of the buffer's tile in TMEM
+  uint64_t* p_full = s_full + kSBufs;  // [3]   P of the buffer's tile in TMEM (128 arrivals)
+  uint64_t* sp_free = p_full + kSBufs; // [3]   PV of the buffer's tile done: buffer reusable, O
                                        //       holds every PV up to that tile
-  uint64_t* stg_full = s_full + 6;     // [2]   staging buffer written (128 arrivals)
-  uint64_t* stg_free = s_full + 8;     // [2]   staging buffer read by its store
-  uint64_t* q_full = s_full + 10;      //       the unit's Q box landed
-  uint64_t* q_empty = s_full + 11;     //       every QK^T of the unit done
-  uint64_t* o_free = s_full + 12;      //       O read out by the epilogue (128 arrivals)
-  uint64_t* done_bar = s_full + 13;    //       every MMA of the CTA done
-  volatile int* abort_flag = reinterpret_cast<int*>(s_full + 14);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 15);
+  uint64_t* q_full = sp_free + kSBufs; //       the unit's Q tile landed (TMA bytes)
+  uint64_t* q_empty = q_full + 1;      //       every QK^T of the unit done
+  uint64_t* o_free = q_full + 2;       //       O read out by the epilogue (128 arrivals)
+  uint64_t* done_bar = q_full + 3;     //       every MMA of the CTA done
+  volatile int* abort_flag = reinterpret_cast<int*>(q_full + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 5);
   // Phase discipline: a thread waits on phase j of a barrier only once it knows phase j - 1 has
-  // completed and while phase j + 1 cannot have (a parity wait cannot tell them apart). The
-  // softmax threads therefore track PV completion through sp_free[y % 2]: once S(g) has landed,
-  // PV(g - 2) is known complete (QK(g) waited for it), so PV(g - 1) is exactly one phase ahead.
+  // completed and while phase j + 1 cannot have (a parity wait cannot tell them apart). The MMA
+  // warp issues QK^T and PV in order, so it tests a slot's half only after the half a ring length
+  // earlier was consumed. With three S/P buffers, QK(x) waits for PV(x - 3); the softmax threads
+  // track PV completion through sp_free[y % 3]: once S(g) has landed, PV(g - 3) is known complete,
+  // so PV(g - 1) is exactly one phase ahead on its buffer.
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&sp_free[i], 1);
-      mbar_init(&stg_full[i], kSoftmaxThreads);
-      mbar_init(&stg_free[i], 1);
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -359,154 +404,170 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int Rt = min(p.rows, kMmaM / G);                 // query rows per M tile
   const int m_tiles = (p.rows + Rt - 1) / Rt;
   const int n_units = p.header[0] * p.h_kv * m_tiles;
+  const uint32_t q_bytes = static_cast<uint32_t>(QA) * 64u * static_cast<uint32_t>(G * Rt) * 2u;
 
-  if (warp == 4) {
-    // ======================================================== TMA producer (one thread)
-    if (lane == 0) {
-      TileIter qi, ki, vi;
-      qi.begin(p, m_tiles, n_units);
-      ki.begin(p, m_tiles, n_units);
-      vi.begin(p, m_tiles, n_units);
-      bool ok = true;
-      uint64_t idle_since = 0;
-      while (!vi.done) {
-        bool moved = false;
-        // the unit's Q box, once every QK^T of the previous unit is done
-        if (!qi.done && (qi.k == 0 || mbar_test(q_empty, (qi.k - 1) & 1u))) {
-          mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(D / 64) * 64u * G * Rt * 2u);
-#pragma unroll
-          for (int a = 0; a < D / 64; ++a)
-            tma_load_4d(q_s + a * (kMmaM * 128), &maps.q, a * 64, qi.mu.h * G, qi.mu.mt * Rt, qi.mu.b, q_full);
-          qi.next_unit(p, m_tiles, n_units);
-          moved = true;
+  if (warp == 4 || warp == 6) {
+    // ======================================================== TMA producers, one warp per ring:
+    // warp 4 fills the K ring, warp 6 the V ring, each in tile order. Lane 0 waits and issues;
+    // the warp's lanes fetch the block table a chunk ahead.
+    const bool is_k = warp == 4;
+    const int NR = is_k ? NK : NV;
+    char* rbase = is_k ? kring : vring;
+    uint64_t* rfull = is_k ? kfull : vfull;
+    uint64_t* rempty = is_k ? kempty : vempty;
+    const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+    bool ok = true;
+    uint32_t i = 0;   // ring ordinal
+    TileIter it;
+    it.begin(p, m_tiles, n_units, HI);
+    PageStream ps;
+    if (!it.done) ps.start(p, it, lane);
+    while (!it.done && ok) {
+      const int t = it.t;
+      const int row0 = tile_row(p, it.mu, it.mu.start + t * kMmaN, ps.page(t), lane == 0 && is_k);
+      for (int j = 0; j < HI; ++j, ++i) {
+        int r = 1;
+        if (lane == 0 && i >= static_cast<uint32_t>(NR)) r = bwait(&rempty[i % NR], (i / NR - 1) & 1u, abort_flag);
+        if (!__shfl_sync(0xffffffffu, r, 0)) {
+          ok = false;
+          break;
         }
-        // K tile x into slot x % NS once the QK^T of tile x - NS is done
-        if (!ki.done && (ki.x < static_cast<uint32_t>(NS) || mbar_test(&k_empty[ki.x % NS], (ki.x / NS - 1) & 1u))) {
-          const int row0 = tile_row(p, ki.mu, ki.mu.start + ki.t * kMmaN);
-          uint64_t* bar = &k_full[ki.x % NS];
-          char* dst = k_s + (ki.x % NS) * C::kTileBytes;
-          mbar_arrive_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-          for (int a = 0; a < D / 64; ++a) tma_load_2d(dst + a * (kMmaN * 128), &maps.k, a * 64, row0, bar);
-          ki.next_tile(p, m_tiles, n_units);
-          moved = true;
-        }
-        // V tile y into slot y % NS once the PV of tile y - NS is done
-        if (!vi.done && vi.x < ki.x &&
-            (vi.x < static_cast<uint32_t>(NS) || mbar_test(&v_empty[vi.x % NS], (vi.x / NS - 1) & 1u))) {
-          const int row0 = tile_row(p, vi.mu, vi.mu.start + vi.t * kMmaN);
-          uint64_t* bar = &v_full[vi.x % NS];
-          char* dst = v_s + (vi.x % NS) * C::kTileBytes;
-          mbar_arrive_expect_tx(bar, C::kTileBytes);
-#pragma unroll
-          for (int a = 0; a < D / 64; ++a) tma_load_2d(dst + a * (kMmaN * 128), &maps.v, a * 64, row0, bar);
-          vi.next_tile(p, m_tiles, n_units);
-          moved = true;
-        }
-        if (moved) {
-          idle_since = 0;
-        } else {
-          const uint64_t now = global_timer_ns();
-          if (idle_since == 0) idle_since = now;
-          if (*abort_flag || now - idle_since > kWaitLimitNs) {
-            ok = false;
-            break;
-          }
-          __nanosleep(64);
+        if (lane == 0) {
+          char* dst = rbase + (i % NR) * kSlotBytes;
+          mbar_arrive_expect_tx(&rfull[i % NR], kSlotBytes);
+          tma_load_2d(dst, map, (2 * j) * 64, row0, &rfull[i % NR]);
+          tma_load_2d(dst + kMmaN * 128, map, (2 * j + 1) * 64, row0, &rfull[i % NR]);
         }
       }
+      if (!ok) break;
+      it.next_tile(p);
+      if (!it.done && (it.t & 31) == 0) ps.advance(p, it, lane);
+    }
+    if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, NBX_DEV_TIMEOUT);
       }
       // the copies issued last have landed before the CTA can exit
-      for (uint32_t j = ki.x > static_cast<uint32_t>(NS) ? ki.x - NS : 0; j < ki.x; ++j)
-        mbar_wait(&k_full[j % NS], (j / NS) & 1u, 100000000ull);
-      for (uint32_t j = vi.x > static_cast<uint32_t>(NS) ? vi.x - NS : 0; j < vi.x; ++j)
-        mbar_wait(&v_full[j % NS], (j / NS) & 1u, 100000000ull);
-      if (qi.k > 0) mbar_wait(q_full, (qi.k - 1) & 1u, 100000000ull);
+      for (uint32_t j = i > static_cast<uint32_t>(NR) ? i - NR : 0; j < i; ++j)
+        mbar_wait(&rfull[j % NR], (j / NR) & 1u, 100000000ull);
     }
     __syncwarp();
   } else if (warp == 5) {
     // ======================================================== MMA issuer (lane 0 decides and issues)
     constexpr uint32_t kIdescS = mma_idesc(kMmaM, kMmaN, false);
-    constexpr uint32_t kIdescO = mma_idesc(kMmaM, D, true);
+    constexpr uint32_t kIdescO = mma_idesc(kMmaM, 128, true);
     const uint32_t q_addr = smem_u32(q_s);
-    TileIter qk, pv;
-    qk.begin(p, m_tiles, n_units);
-    pv.begin(p, m_tiles, n_units);
+    TileIter qk, pv, ql;   // QK^T stream, PV stream, Q loads
+    qk.begin(p, m_tiles, n_units, HI);
+    pv.begin(p, m_tiles, n_units, HI);
+    ql.begin(p, m_tiles, n_units, HI);
+    auto load_q = [&]() {   // ql's unit's Q tile into q_s (lane 0)
+      mbar_arrive_expect_tx(q_full, q_bytes);
+#pragma unroll
+      for (int a = 0; a < QA; ++a)
+        tma_load_4d(q_s + a * (kMmaM * 128), &maps.q, a * 64, ql.mu.h * G, ql.mu.mt * Rt, ql.mu.b, q_full);
+    };
+    if (!ql.done) {
+      if (lane == 0) load_q();
+      ql.next_unit(p);
+    }
     bool ok = true;
     uint64_t idle_since = 0;
+    uint32_t sx = 0, sxp = 0;   // QK^T buffer (x % 3) and its phase count (x / 3)
+    uint32_t sy = 0, syp = 0;   // PV buffer (y % 3) and its phase count (y / 3)
     while (!pv.done) {
       bool moved = false;
-      // ---- S(x) = Q K(x)^T: K landed, the S/P buffer's previous PV done, the unit's Q landed
+      // ---- the next unit's Q, once every QK^T of the current unit has completed
       int go = 0;
+      if (lane == 0 && !ql.done && ql.k <= qk.k + 1) go = mbar_test(q_empty, (ql.k - 1) & 1u);
+      if (__shfl_sync(0xffffffffu, go, 0)) {
+        if (lane == 0) load_q();
+        ql.next_unit(p);
+        moved = true;
+      }
+      // ---- S(x) = Q K(x)^T: K landed, the S/P buffer's previous PV done, the unit's Q landed
+      go = 0;
       if (lane == 0 && !qk.done) {
-        const uint32_t x = qk.x;
-        go = mbar_test(&k_full[x % NS], (x / NS) & 1u) && (x < 2 || mbar_test(&sp_free[x & 1u], ((x >> 1) - 1) & 1u)) &&
+        const uint32_t ki = qk.item(qk.t);
+        go = (qk.x < static_cast<uint32_t>(kSBufs) || mbar_test(&sp_free[sx], (sxp - 1) & 1u)) &&
              (qk.t > 0 || mbar_test(q_full, qk.k & 1u));
+        for (int j = 0; j < HI && go; ++j) go = mbar_test(&kfull[(ki + j) % NK], ((ki + j) / NK) & 1u);
       }
       if (__shfl_sync(0xffffffffu, go, 0)) {
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t x = qk.x;
-          const uint32_t kb = smem_u32(k_s + (x % NS) * C::kTileBytes);
+          const uint32_t ki = qk.item(qk.t);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t a = kk >> 2, sub = kk & 3;
+            const uint32_t a = kk >> 2, sub = kk & 3;   // 64-column atom, 16-column step in it
             const uint64_t ad = smem_desc(q_addr + a * (kMmaM * 128) + sub * 32, 16, 1024);
-            const uint64_t bd = smem_desc(kb + a * (kMmaN * 128) + sub * 32, 16, 1024);
-            tc_mma_ss(tmem + (x & 1u) * kMmaN, ad, bd, kIdescS, kk > 0);
+            const uint32_t kb = smem_u32(kring + ((ki + (a >> 1)) % NK) * kSlotBytes) + (a & 1) * (kMmaN * 128);
+            const uint64_t bd = smem_desc(kb + sub * 32, 16, 1024);
+            tc_mma_ss(tmem + sx * kMmaN, ad, bd, kIdescS, kk > 0);
           }
-          tc_commit(&s_full[x & 1u]);
-          tc_commit(&k_empty[x % NS]);
+          tc_commit(&s_full[sx]);
+          for (int j = 0; j < HI; ++j) tc_commit(&kempty[(ki + j) % NK]);
           if (qk.t == qk.mu.tiles - 1) tc_commit(q_empty);
         }
         __syncwarp();
-        qk.next_tile(p, m_tiles, n_units);
+        qk.next_tile(p);
+        if (++sx == kSBufs) {
+          sx = 0;
+          ++sxp;
+        }
         moved = true;
       }
       // ---- O += P(y) V(y): P written, V landed, O read out by the previous unit's epilogue
       go = 0;
       if (lane == 0 && pv.x < qk.x) {
-        const uint32_t y = pv.x;
-        go = mbar_test(&p_full[y & 1u], (y >> 1) & 1u) && mbar_test(&v_full[y % NS], (y / NS) & 1u) &&
-             (pv.t > 0 || pv.k == 0 || mbar_test(o_free, (pv.k - 1) & 1u));
+        const uint32_t vi = pv.item(pv.t);
+        go = mbar_test(&p_full[sy], syp & 1u) && (pv.t > 0 || pv.k == 0 || mbar_test(o_free, (pv.k - 1) & 1u));
+        for (int j = 0; j < HI && go; ++j) go = mbar_test(&vfull[(vi + j) % NV], ((vi + j) / NV) & 1u);
       }
       if (__shfl_sync(0xffffffffu, go, 0)) {
-        const uint32_t y = pv.x;
-        char* vd = v_s + (y % NS) * C::kTileBytes;
+        const uint32_t vi = pv.item(pv.t);
         const int valid = min(kMmaN, pv.mu.end - (pv.mu.start + pv.t * kMmaN));
         const int ksteps = (valid + 15) >> 4;
         if (valid & 15) {   // rows past the split's end inside the last 16-position step
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
           const int r0 = valid, nr = (ksteps << 4) - valid;
-          for (int a = 0; a < D / 64; ++a)
-            for (int i = lane; i < nr * 8; i += 32)
-              *reinterpret_cast<uint4*>(vd + a * (kMmaN * 128) + (r0 + (i >> 3)) * 128 + (i & 7) * 16) = z;
+          for (int j = 0; j < HI; ++j) {
+            char* vd = vring + ((vi + j) % NV) * kSlotBytes;
+            for (int a = 0; a < 2; ++a)
+              for (int e = lane; e < nr * 8; e += 32)
+                *reinterpret_cast<uint4*>(vd + a * (kMmaN * 128) + (r0 + (e >> 3)) * 128 + (e & 7) * 16) = z;
+          }
           fence_proxy_async();
         }
         __syncwarp();
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t vb = smem_u32(vd);
-          const uint32_t pcol = tmem + (y & 1u) * kMmaN;
+          const uint32_t pcol = tmem + sy * kMmaN;
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
+          for (int j = 0; j < HI; ++j) {   // 128 output columns per V half
+            const uint32_t vb = smem_u32(vring + ((vi + j) % NV) * kSlotBytes);
 #pragma unroll
-            for (int kk = 0; kk < kMmaN / 16; ++kk) {
-              if (kk < ksteps) {
-                const uint64_t bd = smem_desc(vb + kk * (16 * 128), kMmaN * 128, 1024);
-                tc_mma_ts(tmem + C::kOCol, pcol + part * (kMmaN / 2) + kk * 8, bd, kIdescO,
-                          !(pv.t == 0 && part == 0 && kk == 0));
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+              for (int kk = 0; kk < kMmaN / 16; ++kk) {
+                if (kk < ksteps) {
+                  const uint64_t bd = smem_desc(vb + kk * (16 * 128), kMmaN * 128, 1024);
+                  tc_mma_ts(tmem + C::kOCol + j * 128, pcol + part * (kMmaN / 2) + kk * 8, bd, kIdescO,
+                            !(pv.t == 0 && part == 0 && kk == 0));
+                }
               }
             }
           }
-          tc_commit(&v_empty[y % NS]);
-          tc_commit(&sp_free[y & 1u]);
+          for (int j = 0; j < HI; ++j) tc_commit(&vempty[(vi + j) % NV]);
+          tc_commit(&sp_free[sy]);
         }
         __syncwarp();
-        pv.next_tile(p, m_tiles, n_units);
+        pv.next_tile(p);
+        if (++sy == kSBufs) {
+          sy = 0;
+          ++syp;
+        }
         moved = true;
       }
       if (moved) {
@@ -526,8 +587,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       *abort_flag = 1;
       if (lane == 0) raise_status(p.status, NBX_DEV_TIMEOUT);
     }
-    // every MMA of this CTA has completed before the TMEM is released
-    if (lane == 0) tc_commit(done_bar);
+    // every MMA of this CTA has completed, and the last Q copy has landed, before the CTA exits
+    if (lane == 0) {
+      tc_commit(done_bar);
+      if (ql.k > 0) mbar_wait(q_full, (ql.k - 1) & 1u, 100000000ull);
+    }
     __syncwarp();
     mbar_wait(done_bar, 0, 100000000ull);
   } else {
@@ -537,21 +601,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int gq = row - rt * G;                  // query head within the KV head's group
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     bool ok = true;
-    uint32_t g = 0, e = 0;
+    uint32_t g = 0;              // tile ordinal
+    uint32_t gb = 0, gp = 0;     // S/P buffer (g % 3) and its phase count (g / 3)
     TileIter it;
-    it.begin(p, m_tiles, n_units);
-    while (!it.done) {
+    it.begin(p, m_tiles, n_units, HI);
+    int pg_cur = it.done ? 0 : chunk_pages(p, it.mu, 0, lane), pg_nxt = 0;   // lane l: page of tile 32c + l
+    while (!it.done && ok) {
       const MmaUnit mu = it.mu;
       const int r = mu.mt * Rt + rt;
       const bool row_ok = rt < Rt && r < p.rows;
       const int pos = mu.len - p.rows + r;   // last position this row sees
       float m_run = -INFINITY, l_run = 0.f;
-      for (int t = 0; t < mu.tiles; ++t, ++g) {
+      uint32_t pb = 0, pp = 0;   // buffer and phase count of the previous tile (g - 1)
+      for (int t = 0; t < mu.tiles; ++t) {
         const int n0 = mu.start + t * kMmaN;
-        const int page = p.block_table[static_cast<int64_t>(mu.b) * p.max_pages + n0 / p.page_tokens];
+        if ((t & 31) == 0 && t + 32 < mu.tiles) pg_nxt = chunk_pages(p, mu, (t >> 5) + 1, lane);
+        const int page = __shfl_sync(0xffffffffu, pg_cur, t & 31);
+        if ((t & 31) == 31) pg_cur = pg_nxt;
         const bool tile_ok = page >= 0 && page < p.num_pages;
-        const uint32_t sbuf = tmem + (g & 1u) * kMmaN;
-        if (!warp_wait(&s_full[g & 1u], (g >> 1) & 1u, abort_flag)) {
+        const uint32_t sbuf = tmem + gb * kMmaN;
+        if (!warp_wait(&s_full[gb], gp & 1u, abort_flag)) {
           ok = false;
           break;
         }
@@ -560,69 +629,98 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
         for (int c = 0; c < kMmaN / 16; ++c) tmem_ld16(lane_base + (sbuf - tmem) + c * 16, sr + c * 16);
         tmem_wait_ld();
-        // ---- mask and row max (log2 units; NaN propagates through the max)
+        // ---- mask, row max of the raw scores (the scale is positive, so it is the max of the
+        // scaled ones; NaN propagates through the max), 8 independent chains
         const int lim = (row_ok && tile_ok) ? min(mu.end - 1, pos) - n0 : -1;   // last visible column
-        float sv[kMmaN];
-        float mx = -INFINITY;
+        if (!__all_sync(0xffffffffu, lim >= kMmaN - 1)) {
 #pragma unroll
-        for (int j = 0; j < kMmaN; ++j) {
-          sv[j] = j <= lim ? __uint_as_float(sr[j]) * p.qk_scale_log2 : -INFINITY;
-          mx = max_nan(mx, sv[j]);
+          for (int j = 0; j < kMmaN; ++j) sr[j] = j <= lim ? sr[j] : 0xff800000u;   // -inf
         }
+        float mxa[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mxa[i] = __uint_as_float(sr[i]);
+#pragma unroll
+        for (int j = 8; j < kMmaN; ++j) mxa[j & 7] = max_nan(mxa[j & 7], __uint_as_float(sr[j]));
+#pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) mxa[i] = max_nan(mxa[i], mxa[i + w]);
+        const float c = p.qk_scale_log2;
+        const float mx = mxa[0] * c;
         const bool grow = !(mx <= m_run + kMmaTau);
         const float m_new = grow ? mx : m_run;
         const float f = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
         if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
           // O holds the PVs of tiles g-t .. g-1: wait for the last, then rescale it in TMEM
-          if (!warp_wait(&sp_free[(g - 1) & 1u], ((g - 1) >> 1) & 1u, abort_flag)) {
+          if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 16; ++c) {
+          for (int cc = 0; cc < D / 16; ++cc) {
             uint32_t ov[16];
-            tmem_ld16(lane_base + C::kOCol + c * 16, ov);
+            tmem_ld16(lane_base + C::kOCol + cc * 16, ov);
             tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-            tmem_st16(lane_base + C::kOCol + c * 16, ov);
+            tmem_st16(lane_base + C::kOCol + cc * 16, ov);
           }
         }
         m_run = m_new;
         l_run *= f;
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;   // all scores -inf: p = 0
-        // ---- P = 2^(s - m) as bf16 P_hi + P_lo over the S columns: hi in [0, 32), lo in [32, 64)
-        float lsum = 0.f;
+        const float nm = (m_run == -INFINITY) ? 0.f : -m_run;   // all scores -inf: p = 0
+        // ---- p = 2^(s c - m); P_hi = p with the low 16 bits cleared, P_lo = (p - P_hi) likewise:
+        // both exact bf16 values, p - P_hi - P_lo < 2^-14 p. Pairs packed with a byte permute
+        // (upper halves), hi over S columns [0, 32), lo over [32, 64).
+        float ls[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ls[i] = 0.f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t wh[16], wl[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = fast_exp2(sv[half * 32 + 2 * i] - m_use);
-            const float p1 = fast_exp2(sv[half * 32 + 2 * i + 1] - m_use);
-            lsum += p0;
-            lsum += p1;
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-            const float2 hf = __bfloat1622float2(hi);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-            wh[i] = *reinterpret_cast<const uint32_t*>(&hi);
-            wl[i] = *reinterpret_cast<const uint32_t*>(&lo);
+            const int j = half * 32 + 2 * i;
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j]), c, nm));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), c, nm));
+            ls[j & 7] += p0;
+            ls[(j + 1) & 7] += p1;
+            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+            wh[i] = __byte_perm(u0, u1, 0x7632);
+            const float l0 = p0 - __uint_as_float(u0 & 0xffff0000u);
+            const float l1 = p1 - __uint_as_float(u1 & 0xffff0000u);
+            wl[i] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
           }
           tmem_st16(lane_base + (sbuf - tmem) + half * 16, wh);
           tmem_st16(lane_base + (sbuf - tmem) + kMmaN / 2 + half * 16, wl);
         }
+#pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) ls[i] += ls[i + w];
+        const float lsum = ls[0];
         l_run += lsum;
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&p_full[g & 1u]);
+        mbar_arrive(&p_full[gb]);
+        pb = gb;
+        pp = gp;
+        ++g;
+        if (++gb == kSBufs) {
+          gb = 0;
+          ++gp;
+        }
       }
       if (!ok) break;
-      // ---- epilogue: O from TMEM once the unit's last PV is done
-      if (!warp_wait(&sp_free[(g - 1) & 1u], ((g - 1) >> 1) & 1u, abort_flag)) {
+      // ---- the unit's last PV is done: O is complete
+      if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
         ok = false;
         break;
       }
+      it.next_unit(p);
+      if (!it.done) pg_cur = chunk_pages(p, it.mu, 0, lane);
+      // ---- epilogue: O from TMEM
       tc_fence_after();
       const bool single = mu.n_splits <= 1;
       const float sc = single ? ((m_run == -INFINITY) ? 0.f : p.v_scale / l_run) : 1.f;
@@ -631,7 +729,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         p.m_part[orow * p.max_splits + mu.s] = m_run;
         p.l_part[orow * p.max_splits + mu.s] = l_run;
       }
-      for (int ch = 0; ch < D / kChunk; ++ch, ++e) {
+      // destination rows of this lane's stores: rows warp*32 + i*4 + lane/8 of the tile (the warp
+      // only ever stores its own 32 rows, so the staging needs no barrier beyond the warp)
+      float* dst[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = warp * 32 + i * 4 + (lane >> 3);
+        const int rtt = rr / G, gg = rr - rtt * G, r2 = mu.mt * Rt + rtt;
+        dst[i] = nullptr;
+        if (rtt < Rt && r2 < p.rows) {
+          const int64_t orow = (static_cast<int64_t>(mu.b) * p.rows + r2) * p.h_q + static_cast<int64_t>(mu.h) * G + gg;
+          dst[i] = single ? p.out + orow * D : p.acc_part + (orow * p.max_splits + mu.s) * D;
+        }
+      }
+      // 32 columns at a time: TMEM -> registers -> the warp's staging rows (16-byte chunks XOR
+      // row) -> coalesced 128-byte row segments; two staging buffers per warp
+      float* wstg = reinterpret_cast<float*>(stg_s) + warp * (2 * 32 * kChunk);
+#pragma unroll 1
+      for (int ch = 0; ch < D / kChunk; ++ch) {
         uint32_t ov[kChunk];
         tmem_ld16(lane_base + C::kOCol + ch * kChunk, ov);
         tmem_ld16(lane_base + C::kOCol + ch * kChunk + 16, ov + 16);
@@ -640,44 +755,29 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           tc_fence_before();
           mbar_arrive(o_free);
         }
-        // staging buffer e % 2 is free once the store of chunk e - 2 has read it
-        if (e >= 2) {
-          if (row == 0) {
-            bulk_wait_read<1>();
-            mbar_arrive(&stg_free[e & 1u]);
-          }
-          if (!warp_wait(&stg_free[e & 1u], ((e >> 1) - 1) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-        }
-        char* buf = stg_s + (e & 1u) * C::kStgBytes;
+        float* buf = wstg + (ch & 1) * (32 * kChunk);
+        __syncwarp();   // the lanes' reads of this buffer two chunks ago are done
 #pragma unroll
         for (int c4 = 0; c4 < kChunk / 4; ++c4)
-          *reinterpret_cast<float4*>(buf + row * (kChunk * 4) + ((c4 ^ (row & 7)) << 4)) =
+          *reinterpret_cast<float4*>(buf + lane * kChunk + ((c4 ^ (lane & 7)) << 2)) =
               make_float4(__uint_as_float(ov[4 * c4]) * sc, __uint_as_float(ov[4 * c4 + 1]) * sc,
                           __uint_as_float(ov[4 * c4 + 2]) * sc, __uint_as_float(ov[4 * c4 + 3]) * sc);
-        fence_proxy_async();
-        mbar_arrive(&stg_full[e & 1u]);
-        if (row == 0) {
-          if (!mbar_wait(&stg_full[e & 1u], (e >> 1) & 1u)) {
-            *abort_flag = 1;
-          } else if (single) {
-            tma_store_4d(&maps.out, buf, ch * kChunk, mu.h * G, mu.mt * Rt, mu.b);
-          } else {
-            tma_store_5d(&maps.part, buf, ch * kChunk, mu.s, mu.h * G, mu.mt * Rt, mu.b);
-          }
-          bulk_commit();
+        __syncwarp();
+        const int c4 = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int lr = i * 4 + (lane >> 3);   // row within the warp's 32
+          if (dst[i] != nullptr)
+            *reinterpret_cast<float4*>(dst[i] + ch * kChunk + c4 * 4) =
+                *reinterpret_cast<const float4*>(buf + lr * kChunk + ((c4 ^ (lr & 7)) << 2));
         }
       }
       if (!ok) break;
-      it.next_unit(p, m_tiles, n_units);
     }
     if (!ok) {
       *abort_flag = 1;
       if (threadIdx.x == 0) raise_status(p.status, NBX_DEV_TIMEOUT);
     }
-    if (row == 0) bulk_wait_all();   // the stores have completed before the grid does
   }
 
   // every role is done and the MMA warp has seen its last MMA complete: release the TMEM
@@ -716,7 +816,7 @@ bool make_maps(MmaMaps* m, const DecodeParams& p) {
   const cuuint32_t G = static_cast<cuuint32_t>(p.group);
   const cuuint32_t Rt = static_cast<cuuint32_t>(p.rows < kMmaM / p.group ? p.rows : kMmaM / p.group);
   const cuuint64_t R = static_cast<cuuint64_t>(p.rows), B = static_cast<cuuint64_t>(p.batch);
-  const cuuint64_t HQ = static_cast<cuuint64_t>(p.h_q), S = static_cast<cuuint64_t>(p.max_splits);
+  const cuuint64_t HQ = static_cast<cuuint64_t>(p.h_q);
   // pools: rows (page * h_kv + h) * page_tokens + position, columns d
   const cuuint64_t pool_dims[2] = {D, static_cast<cuuint64_t>(p.num_pages) * p.h_kv * p.page_tokens};
   const cuuint64_t pool_str[1] = {D * 2};
@@ -725,19 +825,9 @@ bool make_maps(MmaMaps* m, const DecodeParams& p) {
   const cuuint64_t q_dims[4] = {D, HQ, R, B};
   const cuuint64_t q_str[3] = {D * 2, HQ * D * 2, R * HQ * D * 2};
   const cuuint32_t q_box[4] = {64, G, Rt, 1};
-  // out [B][R][h_q][d] fp32
-  const cuuint64_t o_dims[4] = {D, HQ, R, B};
-  const cuuint64_t o_str[3] = {D * 4, HQ * D * 4, R * HQ * D * 4};
-  const cuuint32_t o_box[4] = {static_cast<cuuint32_t>(kChunk), G, Rt, 1};
-  // partials [B][R][h_q][S][d] fp32
-  const cuuint64_t a_dims[5] = {D, S, HQ, R, B};
-  const cuuint64_t a_str[4] = {D * 4, S * D * 4, HQ * S * D * 4, R * HQ * S * D * 4};
-  const cuuint32_t a_box[5] = {static_cast<cuuint32_t>(kChunk), 1, G, Rt, 1};
   return encode(&m->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k_pool, pool_dims, pool_str, pool_box) &&
          encode(&m->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v_pool, pool_dims, pool_str, pool_box) &&
-         encode(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.q, q_dims, q_str, q_box) &&
-         encode(&m->out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.out, o_dims, o_str, o_box) &&
-         encode(&m->part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, p.acc_part, a_dims, a_str, a_box);
+         encode(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.q, q_dims, q_str, q_box);
 }
 
 template <int D>
@@ -771,12 +861,88 @@ bool mma_path_applies(const DecodeParams& p, int q_dtype, int pool_dtype) {
   const int64_t pool_rows = static_cast<int64_t>(p.num_pages) * p.h_kv * p.page_tokens;
   return q_dtype == NBX_BF16 && pool_dtype == NBX_BF16 && (p.d == 128 || p.d == 256) &&
          (p.page_tokens % kMmaN) == 0 && p.group <= kMmaM && p.rows * p.group >= 64 &&
-         pool_rows < (int64_t{1} << 31) - kMmaN;
+         pool_rows < (int64_t{1} << 31) - kMmaN && p.qk_scale_log2 > 0.f;
 }
 
 cudaError_t decode_dispatch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
   if (p.d == 128) return launch_mma<128>(p, grid_limit, stream);
   return launch_mma<256>(p, grid_limit, stream);
 }
+
+// ---- fp8 pools: bf16 copies of the sequences for the tensor-core kernel
+namespace {
+
+constexpr int kWidenThreads = 256;
+
+// One CTA per (sequence b, 64-position page t of the copies, KV head h): the E4M3 codes of K and V
+// at positions 64t .. 64t + 63 (up to the sequence's length), read through the block table and
+// written as bf16 into the copies -- exactly, since every E4M3 value is a bf16 value. The page's
+// table entry is its own index, or -1 when the source page id is outside the pool (its positions
+// then stay masked, as the SIMT kernel skips them). Pages past the length are not touched.
+__global__ void __launch_bounds__(kWidenThreads) widen_kernel(DecodeParams p) {
+  pdl_wait();   // the plan kernel's lengths and the append's positions are visible from here on
+  pdl_launch_dependents();
+  const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.h_kv));
+  const int64_t pg = blockIdx.x / static_cast<unsigned>(p.h_kv);   // b * t64 + t
+  const int b = static_cast<int>(pg / p.t64);
+  const int t = static_cast<int>(pg - static_cast<int64_t>(b) * p.t64);
+  const int L = p.plan[b].len;
+  const int n0 = t * 64;
+  if (n0 >= L) return;
+  const int page = p.block_table[static_cast<int64_t>(b) * p.max_pages + n0 / p.page_tokens];
+  const bool page_ok = page >= 0 && page < p.num_pages;
+  if (threadIdx.x == 0 && h == 0) {
+    p.widen_bt[pg] = page_ok ? static_cast<int32_t>(pg) : -1;
+    if (!page_ok) raise_status(p.status, NBX_DEV_BAD_PAGE);
+  }
+  if (!page_ok) return;
+  const int rows = min(64, L - n0);
+  const int cpr = p.d / 16;   // 16-byte chunks of codes per position
+  const int64_t src_row = (static_cast<int64_t>(page) * p.h_kv + h) * p.page_tokens + (n0 % p.page_tokens);
+  const int64_t dst_row = (pg * p.h_kv + h) * 64;
+  for (int kv = 0; kv < 2; ++kv) {
+    const uint8_t* src = static_cast<const uint8_t*>(kv == 0 ? p.k_pool : p.v_pool) + src_row * p.d;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(kv == 0 ? p.widen_k : p.widen_v) + dst_row * p.d * 2);
+    for (int c = threadIdx.x; c < rows * cpr; c += kWidenThreads) {
+      const uint4 v = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(c) * 16);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 lo = e4m3x2_to_float2(w[i] & 0xffffu);
+        const float2 hi = e4m3x2_to_float2(w[i] >> 16);
+        const __nv_bfloat162 a = __floats2bfloat162_rn(lo.x, lo.y);
+        const __nv_bfloat162 bb = __floats2bfloat162_rn(hi.x, hi.y);
+        o[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
+        o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+      }
+      dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+}  // namespace
+
+bool widen_path_applies(int q_dtype, int pool_dtype, int rows, int h_q, int h_kv, int d, int page_tokens) {
+  const int group = h_q / h_kv;
+  return q_dtype == NBX_BF16 && pool_dtype == NBX_E4M3 && (d == 128 || d == 256) && (page_tokens % kMmaN) == 0 &&
+         group <= kMmaM && rows * group >= 64;
+}
+
+cudaError_t decode_dispatch_widened(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
+  const int64_t blocks = static_cast<int64_t>(p.batch) * p.t64 * p.h_kv;
+  cudaError_t e = launch_pdl(widen_kernel, static_cast<unsigned>(blocks), kWidenThreads, 0, stream, p);
+  if (e != cudaSuccess) return e;
+  DecodeParams w = p;   // the tensor-core kernel on the copies: 64-position pages, identity table
+  w.k_pool = p.widen_k;
+  w.v_pool = p.widen_v;
+  w.block_table = p.widen_bt;
+  w.max_pages = p.t64;
+  w.page_tokens = kMmaN;
+  w.num_pages = p.batch * p.t64;
+  return decode_dispatch_mma(w, grid_limit, stream);
+}
+
 
 }  // namespace nbx

@@ -48,10 +48,13 @@ struct SeqPlan {
   int32_t pad;
 };
 
-// One (sequence, split) of the work list; a work unit is (entry, KV head, row block).
+// One (sequence, split) of the work list; a work unit is (entry, KV head, row block). The
+// sequence's length and split count ride along, so a unit is described by one 32-byte load.
 struct Entry {
   int32_t b, s, start, end;
+  int32_t len, n_splits, pad0, pad1;
 };
+static_assert(sizeof(Entry) == 32, "Entry is one 32-byte load");
 
 // Byte offsets of the workspace sections (each 256-byte aligned).
 struct WorkspaceLayout {
@@ -61,13 +64,18 @@ struct WorkspaceLayout {
   size_t m_part;    // f32[batch * rows * h_q * max_splits]   (log2 units)
   size_t l_part;    // f32[batch * rows * h_q * max_splits]
   size_t acc_part;  // f32[batch * rows * h_q * max_splits * d]
+  // bf16 copies of an fp8 pool's sequences for the tensor-core kernel (present only when asked
+  // for): [batch * t64][h_kv][64][d] for K and for V, and their page table int32[batch][t64]
+  size_t widen_k, widen_v, widen_bt;
   size_t total;
+  int t64;          // 64-position pages per sequence in the copies (0: no copies)
   int max_splits;
   int row_blocks;
 };
 
 // Returns false if the sizes overflow.
-bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* out);
+bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* out,
+                      bool widen = false);
 
 int splits_for(int length);
 
@@ -90,6 +98,11 @@ struct DecodeParams {
   int max_splits, row_blocks;
   float qk_scale_log2;  // scale * k_scale * log2(e): scores in log2 units
   float v_scale;
+  // bf16 copies of an fp8 pool for the tensor-core kernel (null: none)
+  void* widen_k;
+  void* widen_v;
+  int32_t* widen_bt;
+  int t64;
 };
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);
@@ -99,6 +112,13 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
 // positions.
 bool mma_path_applies(const DecodeParams& p, int q_dtype, int pool_dtype);
 cudaError_t decode_dispatch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream);
+
+// fp8 pools with a multi-row window: the same tensor-core kernel runs on bf16 copies of the
+// sequences' K/V, widened into the workspace (every E4M3 value is a bf16 value, so the copies are
+// exact). The copies use 64-position pages [batch * t64][h_kv][64][d]; a page whose source page id
+// is outside the pool is marked -1, so its positions stay masked.
+bool widen_path_applies(int q_dtype, int pool_dtype, int rows, int h_q, int h_kv, int d, int page_tokens);
+cudaError_t decode_dispatch_widened(const DecodeParams& p, int grid_limit, cudaStream_t stream);
 
 // Launch with programmatic dependent launch: the grid may start while the previous kernel in the
 // stream finishes; the kernel orders itself after it with griddepcontrol.wait.

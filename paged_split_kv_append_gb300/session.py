@@ -14,7 +14,8 @@ from typing import Optional
 
 import torch
 
-from . import (nbx_paged_decode_attn, nbx_paged_decode_workspace_bytes, nbx_paged_kv_append)
+from . import (NBX_BF16, NBX_E4M3, NBX_F32, nbx_paged_decode_attn, nbx_paged_decode_workspace_bytes_for,
+               nbx_paged_kv_append)
 
 POOL_TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
 
@@ -31,14 +32,18 @@ def new_pool(num_pages: int, h_kv: int, page_tokens: int, d: int, dtype: str, de
 
 class PagedDecodeSession:
     def __init__(self, *, num_pages: int, h_kv: int, page_tokens: int, d: int, pool_dtype: str, batch: int,
-                 rows: int, h_q: int, max_seq_len: int, device, fill_nan: bool = True):
+                 rows: int, h_q: int, max_seq_len: int, device, fill_nan: bool = True, q_dtype: str = "bf16",
+                 widen: bool = True):
         self.device = torch.device(device)
         self.num_pages, self.h_kv, self.page_tokens, self.d = num_pages, h_kv, page_tokens, d
         self.pool_dtype = pool_dtype
         self.batch, self.rows, self.h_q, self.max_seq_len = batch, rows, h_q, max_seq_len
         self.k_pool = new_pool(num_pages, h_kv, page_tokens, d, pool_dtype, self.device, fill_nan)
         self.v_pool = new_pool(num_pages, h_kv, page_tokens, d, pool_dtype, self.device, fill_nan)
-        ws = nbx_paged_decode_workspace_bytes(batch, rows, h_q, h_kv, d, max_seq_len)
+        codes = {"f32": NBX_F32, "bf16": NBX_BF16, "e4m3": NBX_E4M3}
+        # widen=False sizes the workspace without the bf16 copies an fp8 pool can use on tensor cores
+        ws = nbx_paged_decode_workspace_bytes_for(codes[q_dtype], codes[pool_dtype] if widen else NBX_F32, batch,
+                                                  rows, h_q, h_kv, d, max_seq_len, page_tokens)
         if ws == 0 and batch > 0:
             raise ValueError("invalid decode sizes")
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device)

@@ -109,3 +109,72 @@ def test_missing_page_sets_status_and_spares_other_sequences():
                               case.cfg.page_tokens, case.scale)
     assert np.max(np.abs(out.cpu().numpy()[:1] - ref)) <= 2e-3
     assert np.all(np.isfinite(out.cpu().numpy()[1]))   # the missing pages' positions are skipped
+
+
+@pytest.mark.parametrize("d,h_q,h_kv,page", [(256, 24, 4, 64), (128, 32, 4, 64)])
+def test_one_cta_runs_every_unit(d, h_q, h_kv, page):
+    # many short units (1-4 tiles, 1-3 splits) queued on one CTA, then on a few: every unit-to-unit
+    # handover of the shared-memory rings and TMEM, compared with the oracle and the default grid
+    lens = (1, 17, 64, 65, 130, 200, 257, 700, 64, 129)
+    cfg = tc_config(f"tc_seq_d{d}", len(lens), 16, h_q, h_kv, d, page, ("fixed", lens), 35)
+    case = wl.make_case(cfg, device=DEV)
+    _, ref = run_step(case)
+    for limit in (1, 2, 7):
+        sess, out = run_step(case, grid_limit=limit)
+        assert sess.status_bits() == 0, f"grid limit {limit}: status {sess.status_bits():#x}"
+        assert torch.equal(out, ref), f"grid limit {limit}"
+    check_against_oracle(case, sess, out)
+
+
+def fp8_config(name, lens, seed, rows=16, page=64):
+    cfg = wl.Config(name, len(lens), rows, 24, 4, 256, page, "e4m3", "bf16", seed, ("fixed", tuple(lens)))
+    kind = nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, rows, 24, 4, 256, 1000, page)
+    assert kind == nbx.PARTIAL_TCGEN05_WIDENED
+    return cfg
+
+
+def test_fp8_pool_window_on_widened_copies():
+    # the copies are exact, so the tensor-core result is held to the bf16 bound, and it agrees with
+    # the SIMT kernel that runs when the workspace has no room for the copies
+    cfg = fp8_config("tc_fp8", (1, 64, 100, 700, 1500), 36)
+    case = wl.make_case(cfg, device=DEV)
+    sess, out = run_step(case)
+    err = check_against_oracle(case, sess, out)
+    assert err <= 2e-3, err
+    simt = bench.session_for_case(case, DEV, widen=False)
+    out_simt = simt.step().clone()
+    torch.cuda.synchronize()
+    assert simt.status_bits() == 0
+    assert float((out - out_simt).abs().max()) <= 2e-3
+
+
+def test_fp8_widened_grid_limits_are_bit_exact():
+    cfg = fp8_config("tc_fp8_grid", (130, 1500, 64), 37, rows=32)
+    case = wl.make_case(cfg, device=DEV)
+    _, ref = run_step(case)
+    for limit in (1, 3, 200):
+        sess, out = run_step(case, grid_limit=limit)
+        assert sess.status_bits() == 0
+        assert torch.equal(out, ref), f"grid limit {limit}"
+
+
+def test_fp8_widened_missing_page_and_nan_code():
+    cfg = fp8_config("tc_fp8_bad", (900, 1300), 38)
+    case = wl.make_case(cfg, device=DEV)
+    case.k_raw[int(case.tok_offset[0]) + 500, 2, 7] = float("nan")   # stored as the E4M3 NaN code
+    sess = bench.session_for_case(case, DEV)
+    bt = sess.block_table.clone()
+    bt[1, 3] = -1
+    sess.block_table = bt
+    out = sess.step()
+    torch.cuda.synchronize()
+    assert sess.status_bits() & nbx.DEV_BAD_PAGE
+    o = out.cpu().numpy()
+    G = cfg.group
+    assert np.all(np.isnan(o[0, :, 2 * G:3 * G]))          # every row of sequence 0 sees position 500
+    assert np.all(np.isfinite(o[0, :, :2 * G])) and np.all(np.isfinite(o[1]))
+    kp, vp = pins.oracle_pools(case)
+    ref = op.decode_attention(case.q.float().cpu().numpy()[:1], kp, vp, "e4m3", case.block_table[:1], case.lens[:1],
+                              cfg.page_tokens, case.scale, case.k_scale, case.v_scale)
+    keep = np.isfinite(ref)
+    assert np.max(np.abs(o[:1][keep] - ref[keep])) <= 2e-3
