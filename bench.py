@@ -68,12 +68,24 @@ def session_for_case(case: "wl.Case", device, fill_nan: bool = True, prefill: bo
 
 
 def measured_peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s burst, source): the driver's measurement, else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def attention_flops(case) -> float:
+    """Algorithmic FLOPs of the step's attention: per (sequence, row, query head) that sees n keys,
+    2*d*n for q.K^T and 2*d*n for P.V."""
+    cfg = case.cfg
+    n_vis = 0
+    for L in case.lens.tolist():
+        for r in range(cfg.rows):
+            n_vis += min(max(int(L) - cfg.rows + r + 1, 0), int(L))
+    return 4.0 * cfg.d * cfg.h_q * n_vis
 
 
 def kernel_source_hash() -> str:
@@ -408,10 +420,24 @@ def main():
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    peak, peak_kind = measured_peaks()
+    peak, tflops_peak, peak_kind = measured_peaks()
     ms = r["ms_per_step"]
     value = r["total_bytes"] / (ms * 1e-3) / 1e9
     dec_achieved = r["kv_bytes"] / (r["dec_ms"] * 1e-3) / 1e9
+    flops = attention_flops(case)
+    # the roof that bounds the decode call: tensor throughput when the step's arithmetic intensity
+    # (FLOPs per K/V byte) is above the ridge of the two measured peaks, else HBM bandwidth
+    tensor_bound = flops / r["kv_bytes"] > tflops_peak * 1e12 / (peak * 1e9)
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": round(flops / (r["dec_ms"] * 1e-3) / 1e12, 2), "peak": tflops_peak,
+                "unit": "TFLOP/s", "frac": round(flops / (r["dec_ms"] * 1e-3) / 1e12 / tflops_peak, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, dense bf16 burst)",
+                "algorithmic_flops_per_launch": int(flops)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(dec_achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(dec_achieved / peak, 4), "frac_of_nominal_8000": round(dec_achieved / 8000.0, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                else "fallback 6.8 TB/s"}
     traffic = profiled_traffic(case.cfg.name, r["kv_bytes"])
     if args.cpu_budget > 0:
         leg = OracleLeg(wl.make_case(case.cfg, device="cpu"))
@@ -434,13 +460,10 @@ def main():
         "dtype": "f32",
         "data": "synthetic (seeded: workloads/)",
         "config": config_block(case, args),
-        "roofline": {"bound": "hbm", "kernel": f"decode call (plan_kernel + {r['partial']} + decode_merge_kernel)",
-                     "achieved": round(dec_achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(dec_achieved / peak, 4), "frac_of_nominal_8000": round(dec_achieved / 8000.0, 4),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s",
+        "roofline": {"kernel": f"decode call (plan_kernel + {r['partial']} + decode_merge_kernel)", **roof,
                      "us_per_launch": round(r["dec_ms"] * 1e3, 3), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": int(r["kv_bytes"])},
+                     "algorithmic_bytes_per_launch": int(r["kv_bytes"]),
+                     "kv_gbs": round(dec_achieved, 2)},
         "cpu_baseline": {"value": round(cpu_bytes / cpu_s / 1e9, 4) if cpu_s > 0 else None, "unit": "GB/s",
                          "cores": 1, "kind": "oracle", "sample": cpu_desc,
                          "seconds": round(cpu_s, 3)},
