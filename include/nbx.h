@@ -224,8 +224,9 @@ NBX_API int nbx_paged_decode_partial_kernel(int q_dtype, int pool_dtype, int row
                                             int num_pages, int page_tokens);
 
 /*
- * nbx_set_decode_grid_limit -- cap the number of CTAs nbx_paged_decode_attn launches (0 = the
- * default, two per SM). Process-wide; the output is bit-identical for every value.
+ * nbx_set_decode_grid_limit -- cap the number of CTAs nbx_paged_decode_attn launches for its split
+ * partial (0 = each kernel's default: two or three CTAs per SM for the SIMT kernel, one per SM for
+ * the tensor-core kernel). Process-wide; the output is bit-identical for every value.
  */
 NBX_API void nbx_set_decode_grid_limit(int max_ctas);
 

@@ -8,36 +8,35 @@
 // nbxtensor/ops/attention_wrappers.py, _math_attention, and as TensorFold PR #1219 ("Gotchas")
 // describes for its attn_rows kernel: each K/V tile is read once for all rows of a stream.
 //
-// GB300 design (one CTA per SM, 7 warps):
+// GB300 design (one CTA per SM, 8 warps):
 //  * Work unit = (split entry, KV head, M tile), M tile fastest. An M tile holds Rt whole query
 //    rows x the G query heads of the KV head (Rt = min(rows, 128 / G)), so its Q block is a box
-//    of a 4-D tensor map. Static round-robin over the plan's longest-first list; the next unit's
-//    work-list entry is loaded one unit ahead.
+//    of a 4-D tensor map. Static round-robin over the plan's longest-first list.
 //  * Shared memory: the unit's Q tile (128-byte-swizzled K-major atoms of 64 columns), a K ring and
 //    a V ring of 16 KB slots (64 positions x 128 columns: half of a d=256 tile, a whole d=128
-//    tile; a tile is one page or a 64-aligned part of one), and per-warp epilogue staging. Every
-//    slot has a full barrier (TMA bytes) and an empty barrier (its consumer).
+//    tile; a tile is one page or a 64-aligned part of one). Every slot has a full barrier (TMA bytes) and an empty barrier (its consumer).
 //  * warps 4 and 6 (producers) fill the K ring and the V ring with TMA (cp.async.bulk.tensor),
 //    one thread issuing while the warp's lanes fetch block-table ids a chunk ahead. A page id
 //    outside the pool loads rows before the tensor, which read as zeros; its positions are
 //    masked. K halves free their slots at QK^T and V halves at PV, so the K stream runs ahead.
 //  * TMEM (512 columns): three S/P buffers [0, 192), O [192, 192 + d). Three buffers let QK^T run
-//    two tiles ahead of PV, which hides the completion latency of the tcgen05.commit hand-offs.
-//  * warp 5 (MMA) holds the TMEM; an event loop issues, as soon as their inputs are ready,
-//      S[x % 3] = Q K(x)^T                    M=128, N=64, K=d; Q and K from shared memory
-//      O       += P_hi(y) V(y) + P_lo(y) V(y)  M=128, N=128 per V half, K=64; P from TMEM
-//    (kind::f16, bf16 x bf16 -> fp32 in TMEM), loads the next unit's Q tile by TMA once the
-//    current unit's last QK^T has completed, and signals completions with tcgen05.commit. P
+//    two tiles ahead of PV.
+//  * Two issuing threads share the tensor pipe, each a plain sequence of bounded waits and MMAs
+//    (kind::f16, bf16 x bf16 -> fp32 in TMEM, completions signalled with tcgen05.commit):
+//      warp 5:  S[x % 3] = Q K(x)^T   M=128, N=64, K=d; Q and K from shared memory; it also loads
+//               each unit's Q tile by TMA once the previous unit's last QK^T has completed
+//      warp 7:  O += P_hi(y) V(y) + P_lo(y) V(y)   M=128, N=d (both V halves in one MMA), K=64;
+//               P from TMEM. It zeroes V rows past a split's end before their PV (0 x NaN would
+//               otherwise leak) and skips 16-position steps that hold none.
+//    Split between two threads, the per-tile control work of one overlaps the other's MMAs. P
 //    enters the product as two bf16 terms, P_hi = p truncated to bf16 and P_lo = (p - P_hi)
-//    truncated, so the weights keep 15 bits or more. The warp zeroes V rows past a split's end
-//    before their PV (0 x NaN would otherwise leak) and skips 16-position steps that hold none.
+//    truncated, so the weights keep 15 bits or more.
 //  * warps 0-3 (softmax, one query vector per thread = one TMEM lane): read S from TMEM, mask
 //    (split end, causal row position, missing pages), run the online softmax in log2 units with
 //    the lazy rescale (O is rescaled in TMEM only when a row's max grows by more than 2^8), and
-//    write P_hi / P_lo over the S columns they came from. After the unit's last PV they store O:
-//    each warp moves its 32 TMEM lanes through its own swizzled staging rows in shared memory to
-//    coalesced 128-byte row segments -- the partial, or the normalised output when the sequence
-//    has one split.
+//    write P_hi / P_lo over the S columns they came from. After the unit's last PV each thread
+//    stores its own row of O, 32 columns at a time, from registers with 32-byte stores -- the
+//    partial, or the normalised output when the sequence has one split.
 //  * Every wait is bounded. On timeout the kernel records NBX_DEV_TIMEOUT, waits (bounded) for
 //    its copies and MMAs in flight, releases its TMEM and returns.
 #include <atomic>
@@ -52,7 +51,7 @@ namespace {
 
 constexpr int kMmaM = 128;       // TMEM lanes / rows of an M tile
 constexpr int kMmaN = 64;        // positions per K/V tile
-constexpr int kMmaThreads = 224;
+constexpr int kMmaThreads = 256;
 constexpr int kSoftmaxThreads = 128;
 constexpr float kMmaTau = 8.0f;  // lazy-rescale threshold, log2 units
 constexpr int kChunk = 32;       // output columns per epilogue step
@@ -65,19 +64,19 @@ struct MmaCfg {
   static constexpr int kKSlots = D <= 128 ? 5 : 4;         // K ring
   static constexpr int kVSlots = kKSlots;                  // V ring
   static constexpr int kQBytes = kMmaM * D * 2;            // Q tile, D / 64 atoms of 16 KB
-  static constexpr int kStgBytes = 4 * 2 * 32 * kChunk * 4;  // epilogue: 4 warps x 2 buffers x 32 rows
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + kKSlots * kSlotBytes;
-  static constexpr int kStgOff = kVOff + kVSlots * kSlotBytes;
-  static constexpr int kBarOff = kStgOff + kStgBytes;
+  static constexpr int kBarOff = kVOff + kVSlots * kSlotBytes;
   static constexpr int kSmem = kBarOff + 512 + 1024;   // barriers + slack for 1024-byte alignment
   // TMEM columns: S/P buffers [0, 192), O [192, 192 + D)
   static constexpr uint32_t kOCol = kSBufs * kMmaN;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM");
   static_assert(kSmem <= 227 * 1024, "shared memory");
-  static_assert((2 * (kKSlots + kVSlots) + 3 * kSBufs + 6) * 8 <= 512, "barrier area");
+  static_assert((2 * (kKSlots + kVSlots) + 3 * kSBufs + 7) * 8 <= 512, "barrier area");
+  // one PV MMA spans both V halves of a tile: their slots must be adjacent (even ordinals)
+  static_assert(kHalves == 1 || (kVSlots % kHalves) == 0, "V ring length");
 };
 
 struct MmaMaps {
@@ -164,17 +163,11 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
+// 32-byte store of eight floats (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float* dst, const float (&v)[8]) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "f"(v[0]), "f"(v[1]), "f"(v[2]),
+               "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7])
+               : "memory");
 }
 
 // Shared-memory matrix descriptor: start >> 4 in bits [0,14), leading byte offset >> 4 in [16,30),
@@ -343,7 +336,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   char* q_s = smem + C::kQOff;
   char* kring = smem + C::kKOff;
   char* vring = smem + C::kVOff;
-  char* stg_s = smem + C::kStgOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
   uint64_t* kfull = bars;              // [NK]  the K slot's half landed (TMA bytes)
   uint64_t* kempty = kfull + NK;       // [NK]  the K slot's half consumed (its QK^T done)
@@ -356,15 +348,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   uint64_t* q_full = sp_free + kSBufs; //       the unit's Q tile landed (TMA bytes)
   uint64_t* q_empty = q_full + 1;      //       every QK^T of the unit done
   uint64_t* o_free = q_full + 2;       //       O read out by the epilogue (128 arrivals)
-  uint64_t* done_bar = q_full + 3;     //       every MMA of the CTA done
-  volatile int* abort_flag = reinterpret_cast<int*>(q_full + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 5);
+  uint64_t* done_bar = q_full + 3;     //       every PV of the CTA done
+  uint64_t* done_qk = q_full + 4;      //       every QK^T of the CTA done
+  volatile int* abort_flag = reinterpret_cast<int*>(q_full + 5);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 6);
   // Phase discipline: a thread waits on phase j of a barrier only once it knows phase j - 1 has
-  // completed and while phase j + 1 cannot have (a parity wait cannot tell them apart). The MMA
-  // warp issues QK^T and PV in order, so it tests a slot's half only after the half a ring length
-  // earlier was consumed. With three S/P buffers, QK(x) waits for PV(x - 3); the softmax threads
-  // track PV completion through sp_free[y % 3]: once S(g) has landed, PV(g - 3) is known complete,
-  // so PV(g - 1) is exactly one phase ahead on its buffer.
+  // completed and while phase j + 1 cannot have (a parity wait cannot tell them apart). Each
+  // issuer consumes its ring slots in order, so it tests a slot's half only after the half a ring
+  // length earlier was consumed by itself. With three S/P buffers, QK(x) waits for PV(x - 3),
+  // whose successor on that buffer, PV(x), needs QK(x) first; PV(y) waits for P(y), whose
+  // successor P(y + 3) needs QK(y + 3) and so PV(y). The softmax threads track PV completion
+  // through sp_free[y % 3]: once S(g) has landed, PV(g - 3) is known complete, so PV(g - 1) is
+  // exactly one phase ahead on its buffer.
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -386,6 +381,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     mbar_init(q_empty, 1);
     mbar_init(o_free, kSoftmaxThreads);
     mbar_init(done_bar, 1);
+    mbar_init(done_qk, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -454,146 +450,123 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     __syncwarp();
   } else if (warp == 5) {
-    // ======================================================== MMA issuer (lane 0 decides and issues)
-    constexpr uint32_t kIdescS = mma_idesc(kMmaM, kMmaN, false);
-    constexpr uint32_t kIdescO = mma_idesc(kMmaM, 128, true);
-    const uint32_t q_addr = smem_u32(q_s);
-    TileIter qk, pv, ql;   // QK^T stream, PV stream, Q loads
-    qk.begin(p, m_tiles, n_units, HI);
-    pv.begin(p, m_tiles, n_units, HI);
-    ql.begin(p, m_tiles, n_units, HI);
-    auto load_q = [&]() {   // ql's unit's Q tile into q_s (lane 0)
-      mbar_arrive_expect_tx(q_full, q_bytes);
-#pragma unroll
-      for (int a = 0; a < QA; ++a)
-        tma_load_4d(q_s + a * (kMmaM * 128), &maps.q, a * 64, ql.mu.h * G, ql.mu.mt * Rt, ql.mu.b, q_full);
-    };
-    if (!ql.done) {
-      if (lane == 0) load_q();
-      ql.next_unit(p);
-    }
-    bool ok = true;
-    uint64_t idle_since = 0;
-    uint32_t sx = 0, sxp = 0;   // QK^T buffer (x % 3) and its phase count (x / 3)
-    uint32_t sy = 0, syp = 0;   // PV buffer (y % 3) and its phase count (y / 3)
-    while (!pv.done) {
-      bool moved = false;
-      // ---- the next unit's Q, once every QK^T of the current unit has completed
-      int go = 0;
-      if (lane == 0 && !ql.done && ql.k <= qk.k + 1) go = mbar_test(q_empty, (ql.k - 1) & 1u);
-      if (__shfl_sync(0xffffffffu, go, 0)) {
-        if (lane == 0) load_q();
-        ql.next_unit(p);
-        moved = true;
-      }
-      // ---- S(x) = Q K(x)^T: K landed, the S/P buffer's previous PV done, the unit's Q landed
-      go = 0;
-      if (lane == 0 && !qk.done) {
-        const uint32_t ki = qk.item(qk.t);
-        go = (qk.x < static_cast<uint32_t>(kSBufs) || mbar_test(&sp_free[sx], (sxp - 1) & 1u)) &&
-             (qk.t > 0 || mbar_test(q_full, qk.k & 1u));
-        for (int j = 0; j < HI && go; ++j) go = mbar_test(&kfull[(ki + j) % NK], ((ki + j) / NK) & 1u);
-      }
-      if (__shfl_sync(0xffffffffu, go, 0)) {
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t ki = qk.item(qk.t);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t a = kk >> 2, sub = kk & 3;   // 64-column atom, 16-column step in it
-            const uint64_t ad = smem_desc(q_addr + a * (kMmaM * 128) + sub * 32, 16, 1024);
-            const uint32_t kb = smem_u32(kring + ((ki + (a >> 1)) % NK) * kSlotBytes) + (a & 1) * (kMmaN * 128);
-            const uint64_t bd = smem_desc(kb + sub * 32, 16, 1024);
-            tc_mma_ss(tmem + sx * kMmaN, ad, bd, kIdescS, kk > 0);
+    // ======================================================== QK^T issuer and Q loader (lane 0)
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = mma_idesc(kMmaM, kMmaN, false);
+      const uint32_t q_addr = smem_u32(q_s);
+      TileIter it;
+      it.begin(p, m_tiles, n_units, HI);
+      bool ok = true;
+      bool q_pending = false;     // a Q copy is in flight that no wait has seen land
+      uint32_t sx = 0, sxp = 0;   // S/P buffer (x % 3) and its phase count (x / 3)
+      while (!it.done) {
+        if (it.t == 0) {
+          // the unit's Q tile, once every QK^T of the previous unit has completed
+          if (it.k > 0 && !bwait(q_empty, (it.k - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
           }
-          tc_commit(&s_full[sx]);
-          for (int j = 0; j < HI; ++j) tc_commit(&kempty[(ki + j) % NK]);
-          if (qk.t == qk.mu.tiles - 1) tc_commit(q_empty);
+          mbar_arrive_expect_tx(q_full, q_bytes);
+#pragma unroll
+          for (int a = 0; a < QA; ++a)
+            tma_load_4d(q_s + a * (kMmaM * 128), &maps.q, a * 64, it.mu.h * G, it.mu.mt * Rt, it.mu.b, q_full);
+          q_pending = true;
         }
-        __syncwarp();
-        qk.next_tile(p);
+        // S(x) = Q K(x)^T once the buffer's previous PV is done, K(x) has landed and the unit's Q has
+        const uint32_t ki = it.item(it.t);
+        if (it.x >= static_cast<uint32_t>(kSBufs)) ok = bwait(&sp_free[sx], (sxp - 1) & 1u, abort_flag);
+        for (int j = 0; j < HI && ok; ++j) ok = bwait(&kfull[(ki + j) % NK], ((ki + j) / NK) & 1u, abort_flag);
+        if (ok && it.t == 0) {
+          ok = bwait(q_full, it.k & 1u, abort_flag);
+          q_pending = !ok;
+        }
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a = kk >> 2, sub = kk & 3;   // 64-column atom, 16-column step in it
+          const uint64_t ad = smem_desc(q_addr + a * (kMmaM * 128) + sub * 32, 16, 1024);
+          const uint32_t kb = smem_u32(kring + ((ki + (a >> 1)) % NK) * kSlotBytes) + (a & 1) * (kMmaN * 128);
+          const uint64_t bd = smem_desc(kb + sub * 32, 16, 1024);
+          tc_mma_ss(tmem + sx * kMmaN, ad, bd, kIdescS, kk > 0);
+        }
+        tc_commit(&s_full[sx]);
+        for (int j = 0; j < HI; ++j) tc_commit(&kempty[(ki + j) % NK]);
+        if (it.t == it.mu.tiles - 1) tc_commit(q_empty);
         if (++sx == kSBufs) {
           sx = 0;
           ++sxp;
         }
-        moved = true;
+        it.next_tile(p);
       }
-      // ---- O += P(y) V(y): P written, V landed, O read out by the previous unit's epilogue
-      go = 0;
-      if (lane == 0 && pv.x < qk.x) {
-        const uint32_t vi = pv.item(pv.t);
-        go = mbar_test(&p_full[sy], syp & 1u) && (pv.t > 0 || pv.k == 0 || mbar_test(o_free, (pv.k - 1) & 1u));
-        for (int j = 0; j < HI && go; ++j) go = mbar_test(&vfull[(vi + j) % NV], ((vi + j) / NV) & 1u);
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, NBX_DEV_TIMEOUT);
+        // a Q copy in flight has landed before the CTA exits
+        if (q_pending) mbar_wait(q_full, it.k & 1u, 100000000ull);
       }
-      if (__shfl_sync(0xffffffffu, go, 0)) {
-        const uint32_t vi = pv.item(pv.t);
-        const int valid = min(kMmaN, pv.mu.end - (pv.mu.start + pv.t * kMmaN));
+      // every QK^T of this CTA has completed before the TMEM is released
+      tc_commit(done_qk);
+      mbar_wait(done_qk, 0, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp == 7) {
+    // ======================================================== PV issuer (lane 0)
+    if (lane == 0) {
+      // one MMA covers every output column: the two V halves of a d = 256 tile sit in adjacent
+      // ring slots (even ring ordinals, an even ring length), so their four 64-column atoms are
+      // 8 KB apart throughout
+      constexpr uint32_t kIdescO = mma_idesc(kMmaM, D, true);
+      TileIter it;
+      it.begin(p, m_tiles, n_units, HI);
+      bool ok = true;
+      uint32_t sy = 0, syp = 0;   // S/P buffer (y % 3) and its phase count (y / 3)
+      while (!it.done) {
+        // O += P(y) V(y): P written, V landed, O read out by the previous unit's epilogue
+        const uint32_t vi = it.item(it.t);
+        ok = bwait(&p_full[sy], syp & 1u, abort_flag);
+        if (ok && it.t == 0 && it.k > 0) ok = bwait(o_free, (it.k - 1) & 1u, abort_flag);
+        for (int j = 0; j < HI && ok; ++j) ok = bwait(&vfull[(vi + j) % NV], ((vi + j) / NV) & 1u, abort_flag);
+        if (!ok) break;
+        const int valid = min(kMmaN, it.mu.end - (it.mu.start + it.t * kMmaN));
         const int ksteps = (valid + 15) >> 4;
-        if (valid & 15) {   // rows past the split's end inside the last 16-position step
+        char* vd = vring + (vi % NV) * kSlotBytes;
+        if (valid & 15) {   // V rows past the split's end inside the last 16-position step: zeros
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          const int r0 = valid, nr = (ksteps << 4) - valid;
-          for (int j = 0; j < HI; ++j) {
-            char* vd = vring + ((vi + j) % NV) * kSlotBytes;
-            for (int a = 0; a < 2; ++a)
-              for (int e = lane; e < nr * 8; e += 32)
-                *reinterpret_cast<uint4*>(vd + a * (kMmaN * 128) + (r0 + (e >> 3)) * 128 + (e & 7) * 16) = z;
-          }
+          for (int at = 0; at < 2 * HI; ++at)
+            for (int rr = valid; rr < (ksteps << 4); ++rr)
+              for (int e = 0; e < 8; ++e) *reinterpret_cast<uint4*>(vd + at * (kMmaN * 128) + rr * 128 + e * 16) = z;
           fence_proxy_async();
         }
-        __syncwarp();
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t pcol = tmem + sy * kMmaN;
+        const uint32_t pcol = tmem + sy * kMmaN;
+        const uint32_t vb = smem_u32(vd);
 #pragma unroll
-          for (int j = 0; j < HI; ++j) {   // 128 output columns per V half
-            const uint32_t vb = smem_u32(vring + ((vi + j) % NV) * kSlotBytes);
+        for (int part = 0; part < 2; ++part) {   // P_hi, then P_lo
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-              for (int kk = 0; kk < kMmaN / 16; ++kk) {
-                if (kk < ksteps) {
-                  const uint64_t bd = smem_desc(vb + kk * (16 * 128), kMmaN * 128, 1024);
-                  tc_mma_ts(tmem + C::kOCol + j * 128, pcol + part * (kMmaN / 2) + kk * 8, bd, kIdescO,
-                            !(pv.t == 0 && part == 0 && kk == 0));
-                }
-              }
-            }
+          for (int kk = 0; kk < kMmaN / 16; ++kk) {
+            if (kk < ksteps)
+              tc_mma_ts(tmem + C::kOCol, pcol + part * (kMmaN / 2) + kk * 8, smem_desc(vb + kk * (16 * 128), kMmaN * 128, 1024),
+                        kIdescO, !(it.t == 0 && part == 0 && kk == 0));
           }
-          for (int j = 0; j < HI; ++j) tc_commit(&vempty[(vi + j) % NV]);
-          tc_commit(&sp_free[sy]);
         }
-        __syncwarp();
-        pv.next_tile(p);
+        for (int j = 0; j < HI; ++j) tc_commit(&vempty[(vi + j) % NV]);
+        tc_commit(&sp_free[sy]);
         if (++sy == kSBufs) {
           sy = 0;
           ++syp;
         }
-        moved = true;
+        it.next_tile(p);
       }
-      if (moved) {
-        idle_since = 0;
-      } else {
-        const uint64_t now = global_timer_ns();
-        if (idle_since == 0) idle_since = now;
-        const int give_up = *abort_flag || now - idle_since > kWaitLimitNs;
-        if (__shfl_sync(0xffffffffu, give_up, 0)) {
-          ok = false;
-          break;
-        }
-        __nanosleep(32);
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, NBX_DEV_TIMEOUT);
       }
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      if (lane == 0) raise_status(p.status, NBX_DEV_TIMEOUT);
-    }
-    // every MMA of this CTA has completed, and the last Q copy has landed, before the CTA exits
-    if (lane == 0) {
+      // every PV of this CTA has completed before the TMEM is released
       tc_commit(done_bar);
-      if (ql.k > 0) mbar_wait(q_full, (ql.k - 1) & 1u, 100000000ull);
+      mbar_wait(done_bar, 0, 100000000ull);
     }
     __syncwarp();
-    mbar_wait(done_bar, 0, 100000000ull);
   } else {
     // ======================================================== softmax warps (row = threadIdx.x)
     const int row = threadIdx.x;
@@ -720,31 +693,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
       it.next_unit(p);
       if (!it.done) pg_cur = chunk_pages(p, it.mu, 0, lane);
-      // ---- epilogue: O from TMEM
+      // ---- epilogue: O from TMEM. Each thread stores its own row, 32 columns at a time, straight
+      // from registers with 32-byte stores: every store fills whole 32-byte sectors, and nothing
+      // waits on the copy engine, which is busy with the K/V stream.
       tc_fence_after();
       const bool single = mu.n_splits <= 1;
       const float sc = single ? ((m_run == -INFINITY) ? 0.f : p.v_scale / l_run) : 1.f;
-      if (row_ok && !single) {
+      float* dst = nullptr;
+      if (row_ok) {
         const int64_t orow = (static_cast<int64_t>(mu.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mu.h) * G + gq;
-        p.m_part[orow * p.max_splits + mu.s] = m_run;
-        p.l_part[orow * p.max_splits + mu.s] = l_run;
-      }
-      // destination rows of this lane's stores: rows warp*32 + i*4 + lane/8 of the tile (the warp
-      // only ever stores its own 32 rows, so the staging needs no barrier beyond the warp)
-      float* dst[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int rr = warp * 32 + i * 4 + (lane >> 3);
-        const int rtt = rr / G, gg = rr - rtt * G, r2 = mu.mt * Rt + rtt;
-        dst[i] = nullptr;
-        if (rtt < Rt && r2 < p.rows) {
-          const int64_t orow = (static_cast<int64_t>(mu.b) * p.rows + r2) * p.h_q + static_cast<int64_t>(mu.h) * G + gg;
-          dst[i] = single ? p.out + orow * D : p.acc_part + (orow * p.max_splits + mu.s) * D;
+        dst = single ? p.out + orow * D : p.acc_part + (orow * p.max_splits + mu.s) * D;
+        if (!single) {
+          p.m_part[orow * p.max_splits + mu.s] = m_run;
+          p.l_part[orow * p.max_splits + mu.s] = l_run;
         }
       }
-      // 32 columns at a time: TMEM -> registers -> the warp's staging rows (16-byte chunks XOR
-      // row) -> coalesced 128-byte row segments; two staging buffers per warp
-      float* wstg = reinterpret_cast<float*>(stg_s) + warp * (2 * 32 * kChunk);
 #pragma unroll 1
       for (int ch = 0; ch < D / kChunk; ++ch) {
         uint32_t ov[kChunk];
@@ -755,21 +718,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           tc_fence_before();
           mbar_arrive(o_free);
         }
-        float* buf = wstg + (ch & 1) * (32 * kChunk);
-        __syncwarp();   // the lanes' reads of this buffer two chunks ago are done
+        if (dst != nullptr) {
 #pragma unroll
-        for (int c4 = 0; c4 < kChunk / 4; ++c4)
-          *reinterpret_cast<float4*>(buf + lane * kChunk + ((c4 ^ (lane & 7)) << 2)) =
-              make_float4(__uint_as_float(ov[4 * c4]) * sc, __uint_as_float(ov[4 * c4 + 1]) * sc,
-                          __uint_as_float(ov[4 * c4 + 2]) * sc, __uint_as_float(ov[4 * c4 + 3]) * sc);
-        __syncwarp();
-        const int c4 = lane & 7;
+          for (int c8 = 0; c8 < kChunk / 8; ++c8) {
+            float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int lr = i * 4 + (lane >> 3);   // row within the warp's 32
-          if (dst[i] != nullptr)
-            *reinterpret_cast<float4*>(dst[i] + ch * kChunk + c4 * 4) =
-                *reinterpret_cast<const float4*>(buf + lr * kChunk + ((c4 ^ (lr & 7)) << 2));
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(ov[8 * c8 + e]) * sc;
+            st_global_v8(dst + ch * kChunk + c8 * 8, v);
+          }
         }
       }
       if (!ok) break;

@@ -173,10 +173,14 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
-// 2^x with the hardware approximation (relative error ~2^-22; ex2(-inf) = +0).
+// 2^x with the hardware approximation (relative error ~2^-22; ex2(-inf) = +0), results below
+// 2^-126 flushed to +0. Every caller weights terms against a largest weight of at least 1 in the
+// same sum (a softmax weight against the row maximum, a split against the largest split maximum),
+// so a flushed weight is far below the sum's fp32 resolution; without the flush each call carries
+// extra instructions for subnormal results.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
