@@ -233,11 +233,17 @@ def flush_l2(buf: torch.Tensor):
     buf.add_(1)   # writes the whole buffer (twice the L2 size)
 
 
+def replica_seed(cfg, rank: int) -> int:
+    """Seed of rank `rank`'s replica: every rank draws its own batch of the same workload (weak
+    scaling; the path has no exchange step, so the ranks share nothing but the timing reduction)."""
+    return cfg.seed + 1000 * rank
+
+
 def run_gpu(args, rank: int, world: int):
     import paged_split_kv_append_gb300 as nbx
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = wl.CONFIGS[args.config]
-    seed = cfg.seed + 1000 * rank
+    seed = replica_seed(cfg, rank)
     case = wl.make_case(cfg, device=dev, seed=seed)
     sess = session_for_case(case, dev)
     torch.cuda.synchronize()
