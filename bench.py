@@ -8,8 +8,8 @@ Inputs are synthetic and seeded (workloads/), resident in HBM before timing star
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
 
 Prints ONE JSON line. value = K/V bytes read per step / device time per step (GB/s).
-The L2 is flushed (a write of twice its size) before every timed step, outside the
-timed events. `--impl reference` times the float64 CPU oracle on this host instead.
+The L2 is flushed before every timed step, outside the timed events: a buffer of twice
+its size is written, then read back, so no input and no dirty line is cached when the step starts. `--impl reference` times the float64 CPU oracle on this host instead.
 """
 
 from __future__ import annotations
@@ -42,7 +42,8 @@ METRIC = "paged decode attn µs/step and KV-read GB/s (% of GB300 HBM peak)"
 DEFAULT_CONFIG = "single_row"
 KERNEL_SOURCES = ("paged_split_kv_append_gb300/csrc/decode_kernels.cuh",
                   "paged_split_kv_append_gb300/csrc/nbx_device.cuh",
-                  "paged_split_kv_append_gb300/csrc/decode_common.cu")
+                  "paged_split_kv_append_gb300/csrc/decode_common.cu",
+                  "paged_split_kv_append_gb300/csrc/decode_mma.cu")
 
 
 # ------------------------------------------------------------------------------------------ shared set-up
@@ -229,8 +230,12 @@ class OracleLeg:
 
 
 # ------------------------------------------------------------------------------------------ GPU leg
-def flush_l2(buf: torch.Tensor):
-    buf.add_(1)   # writes the whole buffer (twice the L2 size)
+def flush_l2(buf: torch.Tensor, sink: torch.Tensor):
+    """Evict the L2 before a timed step: write the whole buffer (twice the L2 size), then read it
+    back. The write evicts every input; the read evicts the write's own dirty lines, so their
+    write-back to HBM happens here and not inside the timed region."""
+    buf.add_(1)
+    sink.add_(buf.sum())
 
 
 def replica_seed(cfg, rank: int) -> int:
@@ -249,7 +254,8 @@ def run_gpu(args, rank: int, world: int):
     torch.cuda.synchronize()
     kv_bytes = case.kv_bytes()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 1 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = torch.zeros(max(2 * l2, 1 << 20) // 4, dtype=torch.float32, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     # warm-up (also configures the kernels before capture)
@@ -278,13 +284,13 @@ def run_gpu(args, rank: int, world: int):
     with ClockSampler(dev.index) as clocks:
         with torch.cuda.stream(stream):
             for i in range(args.steps):
-                flush_l2(flush)
+                flush_l2(flush, sink)
                 ev[i][0].record(stream)
                 graph.replay()
                 ev[i][1].record(stream)
             # the dominant kernel alone (plan + partial, no append), same flush discipline
             for i in range(args.steps):
-                flush_l2(flush)
+                flush_l2(flush, sink)
                 kev[i][0].record(stream)
                 sess.decode(stream=stream)
                 kev[i][1].record(stream)
@@ -313,7 +319,7 @@ def run_gpu(args, rank: int, world: int):
     e2e_ms = []
     with torch.cuda.stream(stream):
         for i in range(e2e_steps):
-            flush_l2(flush)
+            flush_l2(flush, sink)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             for k, t in host_in.items():
@@ -382,9 +388,9 @@ def config_block(case, args, arm: str = "gpu"):
     return {"workload": cfg.name, "batch": cfg.batch, "rows": cfg.rows, "h_q": cfg.h_q, "h_kv": cfg.h_kv,
             "d": cfg.d, "page_tokens": cfg.page_tokens, "kv_dtype": cfg.pool_dtype, "q_dtype": cfg.q_dtype,
             "seq_lens": f"{lens} seed {cfg.seed}", "kv_bytes_per_step": int(case.kv_bytes()),
-            "l2": "flushed before every timed step (write of 2x L2, outside the events)" if arm == "gpu"
+            "l2": "flushed before every timed step, outside the events: a 2x-L2 buffer written, then read back (no input and no dirty line in L2 when the step starts)" if arm == "gpu"
             else "n/a (CPU)",
-            "step": "append of the step's new positions + split plan + split-KV partial with fused merge"
+            "step": "append of the step's new positions + split plan + split-KV partial + fixed-order merge"
             if arm == "gpu" else "the oracle's append of the new positions + float64 attention, bounded sample",
             "timing": "CUDA events per step around a CUDA-graph replay of the step" if arm == "gpu"
             else "wall clock (time.perf_counter) around each sample"}
