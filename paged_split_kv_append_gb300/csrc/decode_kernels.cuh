@@ -26,8 +26,10 @@
 //    moves only when a pass's max exceeds it by more than kTau, so the rescale branch is rare
 //    and the weights stay below 2^kTau (exact enough in fp32). P*V: each lane owns D/32 output
 //    elements of the 4 vectors.
-//  * Epilogue: the four warps' states are merged in fixed warp order through double-buffered
-//    shared memory behind one bounded barrier. A one-split sequence writes its normalised
+//  * Epilogue: the four warps' states are merged in fixed warp order through shared memory: the
+//    unit's last stage, held back from the producer until the merge has read it (this frees the
+//    room of a fourth stage), or a double-buffered scratch for E4M3 stages, which are too small;
+//    bounded barriers order the writes and reads. A one-split sequence writes its normalised
 //    output; otherwise the unit stores its partial and decode_merge_kernel (launched after it)
 //    merges the splits in ascending order. No atomics on values and fixed reduction orders:
 //    the output is bit-identical under any schedule and any physical page placement.
@@ -66,7 +68,11 @@ struct DecodeCfg {
   static constexpr int kQBytes = kQB * D * QT::kBytes;
   static constexpr int kRedFloats = kConsumerWarps * (kQB * D + 2 * kQB);   // one slot
   static constexpr int kPBufBytes = kConsumerWarps * kPassTok * kQB * 8;      // (p, p) pairs
-  static constexpr int kFixed = 2 * kQBytes + 2 * kRedFloats * 4 + kPBufBytes + 2 * (int)sizeof(UnitMeta) + 2048;
+  // the epilogue's cross-warp scratch lives in the unit's last stage when a stage can hold it (every
+  // format but E4M3), which leaves room for one more stage
+  static constexpr bool kRedInStage = kStageBytes >= kRedFloats * 4;
+  static constexpr int kFixed = 2 * kQBytes + (kRedInStage ? 0 : 2 * kRedFloats * 4) + kPBufBytes +
+                                2 * (int)sizeof(UnitMeta) + 2048;
   // resident CTAs per SM: 3 (2 at head dim 256, where the registers allow no more), fewer when
   // shared memory cannot hold two stages for each of them
   static constexpr int kBlocksBySmem = kSmemPerSm / (kFixed + 2 * kStageBytes + 1024);
@@ -82,7 +88,7 @@ struct DecodeCfg {
 struct SmemLayout {
   char* stages;
   char* qbuf;        // [2][kQBytes]
-  float* red;        // [2][warps][kQB*D acc | kQB m | kQB l]
+  float* red;        // [2][warps][kQB*D acc | kQB m | kQB l], or null when it lives in a stage
   f32x2* pbuf;       // [warps][kPassTok][kQB] (p, p) pairs
   UnitMeta* meta;    // [2]
   int* stage_ok;     // [stages] bit h: tile h of the stage was copied
@@ -98,7 +104,7 @@ template <class C>
 struct Carver {
   static constexpr int r(int b) { return ((b + 127) / 128) * 128; }
   static constexpr int bytes() {
-    return r(C::kStages * C::kStageBytes) + r(2 * C::kQBytes) + r(2 * C::kRedFloats * 4) + r(C::kPBufBytes) +
+    return r(C::kStages * C::kStageBytes) + r(2 * C::kQBytes) + r(C::kRedInStage ? 0 : 2 * C::kRedFloats * 4) + r(C::kPBufBytes) +
            r(2 * (int)sizeof(UnitMeta)) + r(C::kStages * 4) + r(16) + 2 * r(C::kStages * 8) + 2 * r(16) + r(8);
   }
   __device__ static SmemLayout carve(char* base) {
@@ -111,7 +117,7 @@ struct Carver {
     };
     s.stages = take(C::kStages * C::kStageBytes);
     s.qbuf = take(2 * C::kQBytes);
-    s.red = reinterpret_cast<float*>(take(2 * C::kRedFloats * 4));
+    s.red = C::kRedInStage ? nullptr : reinterpret_cast<float*>(take(2 * C::kRedFloats * 4));
     s.pbuf = reinterpret_cast<f32x2*>(take(C::kPBufBytes));
     s.meta = reinterpret_cast<UnitMeta*>(take(2 * sizeof(UnitMeta)));
     s.stage_ok = reinterpret_cast<int*>(take(C::kStages * 4));
@@ -427,6 +433,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
       for (int k = 0; k < VPL / 2; ++k) acc2[i][k] = 0ull;
 
     const int n_stages = (u_end - u_start + C::kStageTok - 1) / C::kStageTok;
+    uint32_t last_stage = 0;   // the unit's last stage: held for the epilogue's scratch
     for (int t = 0; t < n_stages; ++t, ++tile_seq) {
       const uint32_t stage = tile_seq % NS;
       if (!wait_or_abort(&sm.full[stage], (tile_seq / NS) & 1u, abort_flag)) {
@@ -533,12 +540,27 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.empty[stage]);
+      if (!C::kRedInStage || t + 1 < n_stages) {
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+      } else {
+        last_stage = stage;
+      }
     }
     if (!ok) break;
 
-    // ---- epilogue: merge the four warps' states in warp order (double-buffered scratch)
-    float* red = sm.red + slot * C::kRedFloats;
+    // ---- epilogue: merge the four warps' states in warp order, through the unit's last stage (its
+    // K/V are consumed) or a double-buffered scratch
+    float* red;
+    if constexpr (C::kRedInStage) {
+      // every warp has finished reading the stage before any warp writes its state over it
+      if (!csync()) {
+        ok = false;
+        break;
+      }
+      red = reinterpret_cast<float*>(sm.stages + last_stage * C::kStageBytes);
+    } else {
+      red = sm.red + slot * C::kRedFloats;
+    }
     {
       float l_tot = l_run;
       if constexpr (TPG == 2) l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
@@ -593,6 +615,12 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
           p.l_part[prow] = L;
         }
       }
+    }
+    if constexpr (C::kRedInStage) {
+      // the stage goes back to the producer: these generic writes come before its next bulk copy
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[last_stage]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.qempty[slot]);   // the slot's queries and metadata are free again
