@@ -158,6 +158,55 @@ NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int row
                                   int32_t* status, void* stream);
 
 /*
+ * nbx_paged_decode_step -- one decode step with no host-side positions: append, then attend.
+ * (nbxtensor/ops/paged_decode_attn.py, paged_kv_append_step_kernel and paged_lens_advance_kernel:
+ * the step writes at the layer's device length and the length then advances, so a recorded launch
+ * replays unchanged; nbxtensor/ops/attention_wrappers.py, paged_decode_attention for the decode.)
+ *
+ * For each sequence b, with n = lens[b] on entry: the step's new keys and values are written at
+ * positions n .. n + rows - 1 (page block_table[b, pos / page_tokens], slot pos % page_tokens,
+ * cast on store exactly as nbx_paged_kv_append does), then the rows attend exactly as
+ * nbx_paged_decode_attn with seq_lens[b] = n + rows, and lens[b] becomes n + rows. Everything
+ * happens on the stream in that order; the call's arguments are the same at every step, so it
+ * can be captured once in a CUDA graph and replayed.
+ *
+ *   new_k, new_v [device] [batch, rows, h_kv, d] in new_dtype (NBX_F32 or NBX_BF16): row r of
+ *                sequence b is the key/value of query row r (position n + r)
+ *   lens         [device] int32 [batch], read and then advanced by rows (in stream order)
+ *   max_seq_len  host bound on every lens[b] + rows (sizes the splits and the workspace)
+ *   every other argument as for nbx_paged_decode_attn; the workspace is sized by
+ *   nbx_paged_decode_workspace_bytes(_for) with the same sizes.
+ * Device-detected problems set status bits: a position at or past max_seq_len (NBX_DEV_BAD_LEN,
+ * not written), a page id outside the pool (NBX_DEV_BAD_PAGE, not written). The host checks are
+ * those of nbx_paged_decode_attn plus new_dtype; on any failure nothing is launched.
+ * This library addition fuses what the pages run as separate launches.
+ */
+NBX_API int nbx_paged_decode_step(const void* q, int q_dtype, int batch, int rows, int h_q, int d, const void* new_k,
+                                  const void* new_v, int new_dtype, void* k_pool, void* v_pool, int pool_dtype,
+                                  int num_pages, int h_kv, int page_tokens, const int32_t* block_table, int max_pages,
+                                  int32_t* lens, int max_seq_len, float scale, float k_scale, float v_scale,
+                                  float* out, void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * nbx_decode_attn_contiguous -- split-KV decode over a contiguous (non-paged) cache.
+ * (nbxtensor/ops/attention_wrappers.py, _decode_attn_vec: the same split read and fixed-order
+ * merge without a page table.)
+ *
+ * The caches k_cache, v_cache [device] [batch, h_kv, capacity, d] in cache_dtype hold sequence b's
+ * positions 0 .. capacity - 1. That is the pool layout with one page of capacity positions per
+ * sequence, so the call is nbx_paged_decode_attn with num_pages = batch, page_tokens = capacity,
+ * max_pages = 1 and the identity block table (page b for sequence b), which the library writes
+ * into the workspace itself. Same results, rules and errors as nbx_paged_decode_attn;
+ * capacity must be a multiple of NBX_TILE_POSITIONS and >= max_seq_len; the workspace is sized by
+ * nbx_paged_decode_workspace_bytes_for(..., page_tokens = capacity).
+ */
+NBX_API int nbx_decode_attn_contiguous(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
+                                       const void* k_cache, const void* v_cache, int cache_dtype, int h_kv,
+                                       int capacity, const int32_t* seq_lens, int max_seq_len, float scale,
+                                       float k_scale, float v_scale, float* out, void* workspace,
+                                       size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * nbx_paged_decode_merge -- the fixed-order merge of split partials on its own.
  * (nbxtensor/ops/attention_wrappers.py, decode_reduce; TensorFold PR #1219, the merge's skip rule.)
  *

@@ -139,13 +139,16 @@ def split_plan(length: int, page_tokens: int) -> tuple[int, int]:
 
     nbxtensor/ops/paged_decode_attn.py, ``paged_decode_splits``: splits =
     max(1, min(ceil(len / 256), 64)). The positions per split are ceil(len / splits)
-    rounded up to a whole page, so no split starts inside a page (the same file,
-    ``paged_decode_attn_split_kernel``: seg_len = ceil(ceil(len / splits) / ALIGN) * ALIGN,
-    with the alignment taken as the page). Split s covers [s*seg, min((s+1)*seg, len));
+    rounded up to a multiple of the alignment A (the same file,
+    ``paged_decode_attn_split_kernel``: seg_len = ceil(ceil(len / splits) / ALIGN) * ALIGN).
+    A is the page when a page holds at most 256 positions, so no split starts inside a page,
+    and 256 for larger pages (a contiguous cache read as one page per sequence), where a
+    256-aligned start is still a tile start. Split s covers [s*seg, min((s+1)*seg, len));
     the last splits may be empty."""
     splits = max(1, min(-(-max(int(length), 1) // SPLIT_POSITIONS), MAX_SPLITS))
+    align = page_tokens if page_tokens <= SPLIT_POSITIONS else SPLIT_POSITIONS
     seg = -(-int(length) // splits)
-    seg = -(-seg // page_tokens) * page_tokens
+    seg = -(-seg // align) * align
     return splits, seg
 
 

@@ -65,6 +65,12 @@ def _declare(l):
     l.nbx_paged_decode_attn.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp, i32, vp, i32,
                                         f32, f32, f32, vp, vp, sz, vp, vp]
     l.nbx_paged_decode_attn.restype = i32
+    l.nbx_paged_decode_step.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, vp, i32, i32, i32, i32, vp, i32,
+                                        vp, i32, f32, f32, f32, vp, vp, sz, vp, vp]
+    l.nbx_paged_decode_step.restype = i32
+    l.nbx_decode_attn_contiguous.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, i32, vp, i32, f32, f32, f32,
+                                             vp, vp, sz, vp, vp]
+    l.nbx_decode_attn_contiguous.restype = i32
     l.nbx_paged_decode_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
     l.nbx_paged_decode_merge.restype = i32
     l.nbx_paged_decode_partial_kernel.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
@@ -194,6 +200,75 @@ def nbx_paged_decode_attn(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.T
                                      float(v_scale), _ptr(out), _ptr(workspace), workspace.numel(),
                                      _ptr(status), _stream(stream))
     _check("nbx_paged_decode_attn", st)
+    return out
+
+
+def nbx_paged_decode_step(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.Tensor, k_pool: torch.Tensor,
+                          v_pool: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor, max_seq_len: int,
+                          scale: float, k_scale: float = 1.0, v_scale: float = 1.0, out: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """One decode step: new_k/new_v [batch, rows, h_kv, d] (fp32 or bf16) are written at positions
+    lens[b] .. lens[b] + rows - 1, the rows of q [batch, rows, h_q, d] attend, and lens [batch] int32
+    advances by rows, all on the stream. Returns out [batch, rows, h_q, d] fp32."""
+    for n, t in (("q", q), ("new_k", new_k), ("new_v", new_v), ("k_pool", k_pool), ("v_pool", v_pool),
+                 ("block_table", block_table), ("lens", lens)):
+        _cuda_contig(n, t)
+    if block_table.dtype != torch.int32 or lens.dtype != torch.int32:
+        raise ValueError("block_table and lens must be int32")
+    if k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype or new_k.shape != new_v.shape or \
+            new_k.dtype != new_v.dtype:
+        raise ValueError("k/v tensors must match")
+    batch, rows, h_q, d = q.shape
+    num_pages, h_kv, page_tokens, d_p = k_pool.shape
+    if d_p != d or tuple(new_k.shape) != (batch, rows, h_kv, d) or block_table.dim() != 2 or \
+            block_table.shape[0] != batch or lens.numel() != batch:
+        raise ValueError(f"q {list(q.shape)}, new_k {list(new_k.shape)}, pool {list(k_pool.shape)}, "
+                         f"block_table {list(block_table.shape)}, lens {list(lens.shape)} do not fit")
+    if out is None:
+        out = torch.empty((batch, rows, h_q, d), dtype=torch.float32, device=q.device)
+    _cuda_contig("out", out)
+    need = nbx_paged_decode_workspace_bytes_for(dtype_code(q), dtype_code(k_pool), batch, rows, h_q, h_kv, d,
+                                                max_seq_len, page_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().nbx_paged_decode_step(_ptr(q), dtype_code(q), batch, rows, h_q, d, _ptr(new_k), _ptr(new_v),
+                                     dtype_code(new_k), _ptr(k_pool), _ptr(v_pool), dtype_code(k_pool), num_pages,
+                                     h_kv, page_tokens, _ptr(block_table), block_table.shape[1], _ptr(lens),
+                                     int(max_seq_len), float(scale), float(k_scale), float(v_scale), _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _check("nbx_paged_decode_step", st)
+    return out
+
+
+def nbx_decode_attn_contiguous(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, seq_lens: torch.Tensor,
+                               max_seq_len: int, scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
+                               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                               status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """q [batch, rows, h_q, d], caches [batch, h_kv, capacity, d] (no page table), seq_lens [batch]
+    int32 -> out [batch, rows, h_q, d] fp32."""
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("seq_lens", seq_lens)):
+        _cuda_contig(n, t)
+    if seq_lens.dtype != torch.int32:
+        raise ValueError("seq_lens must be int32")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must match")
+    batch, rows, h_q, d = q.shape
+    b_c, h_kv, capacity, d_c = k_cache.shape
+    if b_c != batch or d_c != d or seq_lens.numel() != batch:
+        raise ValueError(f"q {list(q.shape)}, cache {list(k_cache.shape)}, seq_lens {list(seq_lens.shape)} do not fit")
+    if out is None:
+        out = torch.empty((batch, rows, h_q, d), dtype=torch.float32, device=q.device)
+    _cuda_contig("out", out)
+    need = nbx_paged_decode_workspace_bytes_for(dtype_code(q), dtype_code(k_cache), batch, rows, h_q, h_kv, d,
+                                                max_seq_len, capacity)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().nbx_decode_attn_contiguous(_ptr(q), dtype_code(q), batch, rows, h_q, d, _ptr(k_cache), _ptr(v_cache),
+                                          dtype_code(k_cache), h_kv, capacity, _ptr(seq_lens), int(max_seq_len),
+                                          float(scale), float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
+                                          workspace.numel(), _ptr(status), _stream(stream))
+    _check("nbx_decode_attn_contiguous", st)
     return out
 
 

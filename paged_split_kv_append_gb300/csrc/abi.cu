@@ -80,7 +80,7 @@ NBX_API int nbx_paged_kv_append(const void* new_k, const void* new_v, int new_dt
   if (n_tok == 0) return NBX_OK;
   if (!new_k || !new_v || !k_pool || !v_pool || !slot_mapping) return NBX_ERR_NULL;
   if (!aligned16(new_k) || !aligned16(new_v) || !aligned16(k_pool) || !aligned16(v_pool)) return NBX_ERR_ALIGN;
-  AppendParams p;
+  AppendParams p = {};
   p.new_k = new_k;
   p.new_v = new_v;
   p.k_pool = k_pool;
@@ -142,12 +142,15 @@ NBX_API size_t nbx_paged_decode_workspace_bytes_for(int q_dtype, int pool_dtype,
   return w.total;
 }
 
-NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
-                                  const void* k_pool, const void* v_pool, int pool_dtype, int num_pages, int h_kv,
-                                  int page_tokens, const int32_t* block_table, int max_pages,
-                                  const int32_t* seq_lens, int max_seq_len, float scale, float k_scale,
-                                  float v_scale, float* out, void* workspace, size_t workspace_bytes,
-                                  int32_t* status, void* stream) {
+// The decode call behind every decode entry point. `identity` reads the pools as one page per
+// sequence through an identity block table the plan kernel writes into the workspace; `lens_out`
+// and `len_add` make it a decode step's (attend with seq_lens + len_add, write that length back).
+static int decode_call(const void* q, int q_dtype, int batch, int rows, int h_q, int d, const void* k_pool,
+                       const void* v_pool, int pool_dtype, int num_pages, int h_kv, int page_tokens,
+                       const int32_t* block_table, int max_pages, const int32_t* seq_lens, int max_seq_len,
+                       float scale, float k_scale, float v_scale, float* out, void* workspace,
+                       size_t workspace_bytes, int32_t* status, cudaStream_t stream, bool identity,
+                       int32_t* lens_out, int len_add) {
   if (!decode_shape_ok(batch, rows, h_q, h_kv, d, max_seq_len)) return NBX_ERR_SHAPE;
   if (num_pages < 1 || page_tokens < 1 || max_pages < 1) return NBX_ERR_SHAPE;
   if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * page_tokens) return NBX_ERR_SHAPE;
@@ -157,7 +160,7 @@ NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int row
   if (!finite(scale) || !finite(k_scale) || !finite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
     return NBX_ERR_VALUE;
   if (batch == 0) return NBX_OK;
-  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !out || !workspace) return NBX_ERR_NULL;
+  if (!q || !k_pool || !v_pool || (!identity && !block_table) || !seq_lens || !out || !workspace) return NBX_ERR_NULL;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return NBX_ERR_ALIGN;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return NBX_ERR_ALIGN;
   WorkspaceLayout w;
@@ -170,12 +173,15 @@ NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int row
   if (widen) w = ww;
 
   char* ws = static_cast<char*>(workspace);
-  DecodeParams p;
+  DecodeParams p = {};
   p.q = q;
   p.k_pool = k_pool;
   p.v_pool = v_pool;
-  p.block_table = block_table;
+  p.ident_bt = identity ? reinterpret_cast<int32_t*>(ws + w.ident_bt) : nullptr;
+  p.block_table = identity ? p.ident_bt : block_table;
   p.seq_lens = seq_lens;
+  p.lens_out = lens_out;
+  p.len_add = len_add;
   p.out = out;
   p.status = status;
   p.header = reinterpret_cast<int32_t*>(ws + w.header);
@@ -202,9 +208,84 @@ NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int row
   p.widen_v = widen ? ws + w.widen_v : nullptr;
   p.widen_bt = widen ? reinterpret_cast<int32_t*>(ws + w.widen_bt) : nullptr;
   p.t64 = w.t64;
-  const cudaError_t e =
-      decode_dispatch(p, q_dtype, pool_dtype, g_grid_limit.load(), static_cast<cudaStream_t>(stream));
+  const cudaError_t e = decode_dispatch(p, q_dtype, pool_dtype, g_grid_limit.load(), stream);
   return e == cudaSuccess ? NBX_OK : NBX_ERR_CUDA;
+}
+
+NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
+                                  const void* k_pool, const void* v_pool, int pool_dtype, int num_pages, int h_kv,
+                                  int page_tokens, const int32_t* block_table, int max_pages,
+                                  const int32_t* seq_lens, int max_seq_len, float scale, float k_scale,
+                                  float v_scale, float* out, void* workspace, size_t workspace_bytes,
+                                  int32_t* status, void* stream) {
+  return decode_call(q, q_dtype, batch, rows, h_q, d, k_pool, v_pool, pool_dtype, num_pages, h_kv, page_tokens,
+                     block_table, max_pages, seq_lens, max_seq_len, scale, k_scale, v_scale, out, workspace,
+                     workspace_bytes, status, static_cast<cudaStream_t>(stream), false, nullptr, 0);
+}
+
+NBX_API int nbx_decode_attn_contiguous(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
+                                       const void* k_cache, const void* v_cache, int cache_dtype, int h_kv,
+                                       int capacity, const int32_t* seq_lens, int max_seq_len, float scale,
+                                       float k_scale, float v_scale, float* out, void* workspace,
+                                       size_t workspace_bytes, int32_t* status, void* stream) {
+  // [batch, h_kv, capacity, d] is the pool layout with one page of `capacity` positions per sequence
+  if (capacity < 1) return NBX_ERR_SHAPE;
+  return decode_call(q, q_dtype, batch, rows, h_q, d, k_cache, v_cache, cache_dtype, batch < 1 ? 1 : batch, h_kv,
+                     capacity, nullptr, 1, seq_lens, max_seq_len, scale, k_scale, v_scale, out, workspace,
+                     workspace_bytes, status, static_cast<cudaStream_t>(stream), true, nullptr, 0);
+}
+
+NBX_API int nbx_paged_decode_step(const void* q, int q_dtype, int batch, int rows, int h_q, int d, const void* new_k,
+                                  const void* new_v, int new_dtype, void* k_pool, void* v_pool, int pool_dtype,
+                                  int num_pages, int h_kv, int page_tokens, const int32_t* block_table, int max_pages,
+                                  int32_t* lens, int max_seq_len, float scale, float k_scale, float v_scale,
+                                  float* out, void* workspace, size_t workspace_bytes, int32_t* status,
+                                  void* stream) {
+  // every check of the decode first, so an invalid call launches nothing
+  if (!decode_shape_ok(batch, rows, h_q, h_kv, d, max_seq_len)) return NBX_ERR_SHAPE;
+  if (new_dtype != NBX_F32 && new_dtype != NBX_BF16) return NBX_ERR_DTYPE;
+  if (num_pages < 1 || page_tokens < 1 || max_pages < 1) return NBX_ERR_SHAPE;
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * page_tokens) return NBX_ERR_SHAPE;
+  if ((page_tokens % NBX_TILE_POSITIONS) != 0) return NBX_ERR_PAGE_ALIGN;
+  if (q_dtype != NBX_F32 && q_dtype != NBX_BF16) return NBX_ERR_DTYPE;
+  if (pool_dtype != NBX_F32 && pool_dtype != NBX_BF16 && pool_dtype != NBX_E4M3) return NBX_ERR_DTYPE;
+  if (!finite(scale) || !finite(k_scale) || !finite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+    return NBX_ERR_VALUE;
+  if (batch == 0) return NBX_OK;
+  if (!q || !new_k || !new_v || !k_pool || !v_pool || !block_table || !lens || !out || !workspace) return NBX_ERR_NULL;
+  if (!aligned16(new_k) || !aligned16(new_v) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      !aligned16(out))
+    return NBX_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return NBX_ERR_ALIGN;
+  WorkspaceLayout w;
+  if (!workspace_layout(batch, rows, h_q, h_kv, d, max_seq_len, &w)) return NBX_ERR_SHAPE;
+  if (workspace_bytes < w.total) return NBX_ERR_WORKSPACE;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the step's rows new positions per sequence, written at lens[b] .. lens[b] + rows - 1
+  AppendParams a = {};
+  a.new_k = new_k;
+  a.new_v = new_v;
+  a.k_pool = k_pool;
+  a.v_pool = v_pool;
+  a.status = status;
+  a.n_tok = batch * rows;
+  a.h_kv = h_kv;
+  a.d = d;
+  a.num_pages = num_pages;
+  a.page_tokens = page_tokens;
+  a.k_inv = 1.0f / k_scale;
+  a.v_inv = 1.0f / v_scale;
+  a.lens = lens;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.rows = rows;
+  a.max_pos = max_seq_len;
+  cudaError_t e = append_dispatch(a, new_dtype, pool_dtype, st);
+  if (e != cudaSuccess) return NBX_ERR_CUDA;
+  // then the decode with the advanced lengths; its plan kernel writes them back to lens
+  return decode_call(q, q_dtype, batch, rows, h_q, d, k_pool, v_pool, pool_dtype, num_pages, h_kv, page_tokens,
+                     block_table, max_pages, lens, max_seq_len, scale, k_scale, v_scale, out, workspace,
+                     workspace_bytes, status, st, false, lens, rows);
 }
 
 NBX_API int nbx_paged_decode_merge(const float* acc_part, const float* m_part, const float* l_part, int n_rows,

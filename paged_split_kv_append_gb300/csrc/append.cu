@@ -1,4 +1,6 @@
-// Kernel 1: the slot-mapping append, cast on store.
+// Kernel 1: the slot-mapping append, cast on store; in decode-step mode the slots come from the
+// device lengths and the block table (nbxtensor/ops/paged_decode_attn.py, paged_kv_append_step_kernel:
+// the step writes at the layer's device length, so a recorded launch replays unchanged).
 //
 // nbxtensor/ops/paged_decode_attn.py, paged_kv_append_kernel: one program per (new token,
 // KV head) writes its D values to pool[slot / page_tokens, h, slot % page_tokens, :], converted
@@ -61,7 +63,23 @@ __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
     const int64_t th = w >> 1;
     const int64_t t = th / p.h_kv;
     const int h = static_cast<int>(th - t * p.h_kv);
-    const int64_t slot = p.slot_mapping[t];
+    int64_t slot;
+    if (p.lens == nullptr) {
+      slot = p.slot_mapping[t];
+    } else {   // decode step: the position comes from the device length, the page from the table
+      const int64_t b = t / p.rows;
+      const int64_t pos = static_cast<int64_t>(p.lens[b]) + (t - b * p.rows);
+      if (pos < 0 || pos >= p.max_pos) {
+        if (lane == 0 && which == 0 && h == 0) raise_status(p.status, NBX_DEV_BAD_LEN);
+        continue;
+      }
+      const int32_t pg = p.block_table[b * p.max_pages + pos / p.page_tokens];
+      if (pg < 0 || pg >= p.num_pages) {
+        if (lane == 0 && which == 0 && h == 0) raise_status(p.status, NBX_DEV_BAD_PAGE);
+        continue;
+      }
+      slot = static_cast<int64_t>(pg) * p.page_tokens + pos % p.page_tokens;
+    }
     if (slot < 0 || slot >= pool_positions) {
       if (lane == 0 && which == 0 && h == 0) raise_status(p.status, NBX_DEV_BAD_SLOT);
       continue;

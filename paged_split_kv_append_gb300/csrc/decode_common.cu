@@ -23,6 +23,8 @@ bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq
   size_t off = 0;
   w->header = off;
   off += up(64 * 4);
+  w->ident_bt = off;
+  off += up(static_cast<size_t>(batch) * 4);
   w->plan = off;
   off += up(static_cast<size_t>(batch) * sizeof(SeqPlan));
   w->entries = off;
@@ -77,7 +79,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   }
   __syncthreads();
   for (int b = tid; b < B; b += kPlanThreads) {
-    int L = p.seq_lens[b];
+    int L = p.seq_lens[b] + p.len_add;   // a decode step attends to its own new positions
+    if (p.ident_bt) p.ident_bt[b] = b;
+    if (p.lens_out) p.lens_out[b] = L;   // the step's length advance; nothing later reads seq_lens
     if (L < 0 || L > p.max_seq_len || static_cast<int64_t>(L) > cap) {
       raise_status(p.status, NBX_DEV_BAD_LEN);
       L = 0;
@@ -85,7 +89,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
     int S = (max(L, 1) + NBX_SPLIT_POSITIONS - 1) / NBX_SPLIT_POSITIONS;
     S = S > NBX_MAX_SPLITS ? NBX_MAX_SPLITS : S;
     int seg = (L + S - 1) / S;
-    seg = ((seg + p.page_tokens - 1) / p.page_tokens) * p.page_tokens;
+    // splits start on whole pages, or on 256-position boundaries when a page is longer (a
+    // contiguous cache read as one page per sequence): tile starts either way
+    const int align = p.page_tokens <= NBX_SPLIT_POSITIONS ? p.page_tokens : NBX_SPLIT_POSITIONS;
+    seg = ((seg + align - 1) / align) * align;
     const int n = L > 0 ? (L + seg - 1) / seg : 0;
     SeqPlan sp;
     sp.len = L;

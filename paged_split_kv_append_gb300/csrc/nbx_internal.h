@@ -30,6 +30,11 @@ struct AppendParams {
   int32_t* status;
   int n_tok, h_kv, d, num_pages, page_tokens;
   float k_inv, v_inv;
+  // decode-step mode (lens != null): token t = b * rows + r goes to position lens[b] + r of
+  // sequence b, its page read from the block table; positions at or past max_pos are refused
+  const int32_t* lens;
+  const int32_t* block_table;
+  int max_pages, rows, max_pos;
 };
 
 cudaError_t append_dispatch(const AppendParams& p, int new_dtype, int pool_dtype, cudaStream_t stream);
@@ -59,6 +64,7 @@ static_assert(sizeof(Entry) == 32, "Entry is one 32-byte load");
 // Byte offsets of the workspace sections (each 256-byte aligned).
 struct WorkspaceLayout {
   size_t header;    // int32[64]: [0] entries in the list, [1] work counter
+  size_t ident_bt;  // int32[batch]: the identity block table of a contiguous cache (row b = page b)
   size_t plan;      // SeqPlan[batch]
   size_t entries;   // Entry[batch * max_splits]
   size_t m_part;    // f32[batch * rows * h_q * max_splits]   (log2 units)
@@ -103,6 +109,12 @@ struct DecodeParams {
   void* widen_v;
   int32_t* widen_bt;
   int t64;
+  // the plan kernel writes ident_bt[b] = b (a contiguous cache read as one page per sequence;
+  // block_table then points at it), and, for a decode step, attends with seq_lens[b] + len_add
+  // and writes that length to lens_out[b] (null: neither)
+  int32_t* ident_bt;
+  int32_t* lens_out;
+  int len_add;
 };
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);

@@ -31,7 +31,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     syms = declared_symbols()
     for s in ("nbx_paged_kv_append", "nbx_paged_decode_workspace_bytes", "nbx_paged_decode_attn",
-              "nbx_paged_decode_merge", "nbx_status_string", "nbx_abi_version", "nbx_set_decode_grid_limit"):
+              "nbx_paged_decode_merge", "nbx_status_string", "nbx_abi_version", "nbx_set_decode_grid_limit",
+              "nbx_paged_decode_step", "nbx_decode_attn_contiguous"):
         assert s in syms
 
 
@@ -99,6 +100,60 @@ def test_decode_host_checks(lib):
     assert _decode(lib, ws=ctypes.c_void_p(0x10010)) == -7   # workspace must be 256-byte aligned
     need = lib.nbx_paged_decode_workspace_bytes(2, 1, 8, 2, 128, 160)
     assert _decode(lib, ws_bytes=need - 1) == -5
+
+
+def _step(lib, **kw):
+    a = dict(q=FAKE, q_dtype=1, batch=2, rows=1, h_q=8, d=128, nk=FAKE, nv=FAKE, new_dtype=0, k_pool=FAKE,
+             v_pool=FAKE, pool_dtype=1, num_pages=100, h_kv=2, page_tokens=16, bt=FAKE, max_pages=10, lens=FAKE,
+             max_seq_len=160, scale=0.1, k_scale=1.0, v_scale=1.0, out=FAKE, ws=FAKE, ws_bytes=1 << 30,
+             status=NULL, stream=NULL)
+    a.update(kw)
+    return lib.nbx_paged_decode_step(a["q"], a["q_dtype"], a["batch"], a["rows"], a["h_q"], a["d"], a["nk"],
+                                     a["nv"], a["new_dtype"], a["k_pool"], a["v_pool"], a["pool_dtype"],
+                                     a["num_pages"], a["h_kv"], a["page_tokens"], a["bt"], a["max_pages"],
+                                     a["lens"], a["max_seq_len"], a["scale"], a["k_scale"], a["v_scale"], a["out"],
+                                     a["ws"], a["ws_bytes"], a["status"], a["stream"])
+
+
+def test_step_host_checks(lib):
+    # every refusal happens before the step's append is launched
+    assert _step(lib, batch=0) == 0
+    assert _step(lib, h_q=6, h_kv=4) == -2
+    assert _step(lib, max_seq_len=161) == -2
+    assert _step(lib, page_tokens=24, max_seq_len=100) == -4
+    assert _step(lib, new_dtype=2) == -3                     # new keys are fp32 or bf16
+    assert _step(lib, pool_dtype=7) == -3
+    assert _step(lib, k_scale=0.0) == -8
+    assert _step(lib, nk=NULL) == -1
+    assert _step(lib, lens=NULL) == -1
+    assert _step(lib, bt=NULL) == -1
+    assert _step(lib, nv=FAKE_ODD) == -7
+    need = lib.nbx_paged_decode_workspace_bytes(2, 1, 8, 2, 128, 160)
+    assert _step(lib, ws_bytes=need - 1) == -5
+
+
+def _contig(lib, **kw):
+    a = dict(q=FAKE, q_dtype=1, batch=2, rows=1, h_q=8, d=128, k=FAKE, v=FAKE, dtype=1, h_kv=2, capacity=160,
+             lens=FAKE, max_seq_len=160, scale=0.1, k_scale=1.0, v_scale=1.0, out=FAKE, ws=FAKE, ws_bytes=1 << 30,
+             status=NULL, stream=NULL)
+    a.update(kw)
+    return lib.nbx_decode_attn_contiguous(a["q"], a["q_dtype"], a["batch"], a["rows"], a["h_q"], a["d"], a["k"],
+                                          a["v"], a["dtype"], a["h_kv"], a["capacity"], a["lens"],
+                                          a["max_seq_len"], a["scale"], a["k_scale"], a["v_scale"], a["out"],
+                                          a["ws"], a["ws_bytes"], a["status"], a["stream"])
+
+
+def test_contiguous_host_checks(lib):
+    assert _contig(lib, batch=0) == 0
+    assert _contig(lib, capacity=0) == -2
+    assert _contig(lib, max_seq_len=161) == -2               # more positions than the cache holds
+    assert _contig(lib, capacity=40, max_seq_len=40) == -4   # capacity: whole 16-position tiles
+    assert _contig(lib, dtype=9) == -3
+    assert _contig(lib, k=NULL) == -1
+    assert _contig(lib, lens=NULL) == -1
+    assert _contig(lib, out=FAKE_ODD) == -7
+    need = lib.nbx_paged_decode_workspace_bytes_for(1, 1, 2, 1, 8, 2, 128, 160, 160)
+    assert _contig(lib, ws_bytes=need - 1) == -5
 
 
 def test_workspace_bytes(lib):

@@ -100,6 +100,15 @@ def test_split_rule():
     assert op.split_plan(257, 16) == (2, 144)
     assert op.split_plan(131072, 16) == (64, 2048)
     assert op.split_plan(32768, 64) == (64, 512)
+    # a page larger than a split (a contiguous cache: one page per sequence) keeps 256-aligned splits
+    for P in (1024, 4096, 1 << 17):
+        for L in (1, 255, 256, 257, 4000, 32768, 131072):
+            if L > P:
+                continue
+            S, seg = op.split_plan(L, P)
+            assert S == max(1, min(-(-max(L, 1) // 256), 64)) and seg % 256 == 0 and S * seg >= L
+    assert op.split_plan(4000, 4096) == (16, 256)
+    assert op.split_plan(32768, 1 << 17) == (64, 512)
     # empty trailing splits exist when rounding to whole pages overshoots
     b = op.split_bounds(16385, 64)
     assert b[-2] == b[-1] == 16385
