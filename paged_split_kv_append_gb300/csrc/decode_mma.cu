@@ -28,9 +28,10 @@
 //      warp 7:  O += P_hi(y) V(y) + P_lo(y) V(y)   M=128, N=d (both V halves in one MMA), K=64;
 //               P from TMEM. It zeroes V rows past a split's end before their PV (0 x NaN would
 //               otherwise leak) and skips 16-position steps that hold none.
-//    Split between two threads, the per-tile control work of one overlaps the other's MMAs. P
-//    enters the product as two bf16 terms, P_hi = p truncated to bf16 and P_lo = (p - P_hi)
-//    truncated, so the weights keep 15 bits or more.
+//    Split between two threads, the per-tile control work of one overlaps the other's MMAs. With
+//    a bf16 pool P enters the product as two bf16 terms, P_hi = p truncated to bf16 and
+//    P_lo = (p - P_hi) truncated, so the weights keep 15 bits or more. With the exact copies of an
+//    fp8 pool V is f16 and P enters as one f16 term rounded to nearest (11 bits), halving PV.
 //  * warps 0-3 (softmax, one query vector per thread = one TMEM lane): read S from TMEM, mask
 //    (split end, causal row position, missing pages), run the online softmax in log2 units with
 //    the lazy rescale (O is rescaled in TMEM only when a row's max grows by more than 2^8), and
@@ -42,6 +43,7 @@
 #include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include "nbx_device.cuh"
 #include "nbx_internal.h"
@@ -182,11 +184,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A and B (bits 7-9,
-// 10-12 = 1), A K-major (bit 15 = 0), B K-major or MN-major (bit 16), N >> 3 in bits 17-22,
-// M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t mma_idesc(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B both bf16 (bits 7-9
+// and 10-12 = 1) or both f16 (0), A K-major (bit 15 = 0), B K-major or MN-major (bit 16), N >> 3 in
+// bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t mma_idesc(int m, int n, bool b_mn_major, bool f16 = false) {
+  const uint32_t fmt = f16 ? 0u : 1u;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
@@ -323,7 +326,9 @@ struct PageStream {
   __device__ __forceinline__ int page(int t) const { return __shfl_sync(0xffffffffu, cur, t & 31); }
 };
 
-template <int D>
+// PvF16: V is f16 (the exact f16 copies of an fp8 pool) and P enters PV as one f16 term, rounded
+// to nearest; otherwise V is bf16 and P enters as P_hi + P_lo.
+template <int D, bool PvF16>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     decode_partial_mma_kernel(DecodeParams p, const __grid_constant__ MmaMaps maps) {
   using C = MmaCfg<D>;
@@ -516,7 +521,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // one MMA covers every output column: the two V halves of a d = 256 tile sit in adjacent
       // ring slots (even ring ordinals, an even ring length), so their four 64-column atoms are
       // 8 KB apart throughout
-      constexpr uint32_t kIdescO = mma_idesc(kMmaM, D, true);
+      constexpr uint32_t kIdescO = mma_idesc(kMmaM, D, true, PvF16);
       TileIter it;
       it.begin(p, m_tiles, n_units, HI);
       bool ok = true;
@@ -542,7 +547,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const uint32_t pcol = tmem + sy * kMmaN;
         const uint32_t vb = smem_u32(vd);
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {   // P_hi, then P_lo
+        for (int part = 0; part < (PvF16 ? 1 : 2); ++part) {   // P_hi, then P_lo (or the one f16 P)
 #pragma unroll
           for (int kk = 0; kk < kMmaN / 16; ++kk) {
             if (kk < ksteps)
@@ -659,14 +664,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), c, nm));
             ls[j & 7] += p0;
             ls[(j + 1) & 7] += p1;
-            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-            wh[i] = __byte_perm(u0, u1, 0x7632);
-            const float l0 = p0 - __uint_as_float(u0 & 0xffff0000u);
-            const float l1 = p1 - __uint_as_float(u1 & 0xffff0000u);
-            wl[i] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
+            if constexpr (PvF16) {   // f16, round to nearest: p - P < 2^-11 p (p <= 2^8 fits)
+              const __half2 h = __floats2half2_rn(p0, p1);
+              wh[i] = *reinterpret_cast<const uint32_t*>(&h);
+            } else {
+              const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+              wh[i] = __byte_perm(u0, u1, 0x7632);
+              const float l0 = p0 - __uint_as_float(u0 & 0xffff0000u);
+              const float l1 = p1 - __uint_as_float(u1 & 0xffff0000u);
+              wl[i] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
+            }
           }
           tmem_st16(lane_base + (sbuf - tmem) + half * 16, wh);
-          tmem_st16(lane_base + (sbuf - tmem) + kMmaN / 2 + half * 16, wl);
+          if constexpr (!PvF16) tmem_st16(lane_base + (sbuf - tmem) + kMmaN / 2 + half * 16, wl);
         }
 #pragma unroll
         for (int w = 4; w > 0; w >>= 1)
@@ -767,7 +777,7 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* ba
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_maps(MmaMaps* m, const DecodeParams& p) {
+bool make_maps(MmaMaps* m, const DecodeParams& p, bool v_f16) {
   const cuuint64_t D = static_cast<cuuint64_t>(p.d);
   const cuuint32_t G = static_cast<cuuint32_t>(p.group);
   const cuuint32_t Rt = static_cast<cuuint32_t>(p.rows < kMmaM / p.group ? p.rows : kMmaM / p.group);
@@ -782,21 +792,23 @@ bool make_maps(MmaMaps* m, const DecodeParams& p) {
   const cuuint64_t q_str[3] = {D * 2, HQ * D * 2, R * HQ * D * 2};
   const cuuint32_t q_box[4] = {64, G, Rt, 1};
   return encode(&m->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k_pool, pool_dims, pool_str, pool_box) &&
-         encode(&m->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v_pool, pool_dims, pool_str, pool_box) &&
+         encode(&m->v, v_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v_pool,
+                pool_dims, pool_str, pool_box) &&
          encode(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.q, q_dims, q_str, q_box);
 }
 
-template <int D>
+template <int D, bool PvF16>
 cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
   using C = MmaCfg<D>;
   static std::atomic<uint64_t> configured{0};   // devices whose shared-memory limit is raised
   MmaMaps maps;
-  if (!make_maps(&maps, p)) return cudaErrorInvalidValue;
+  if (!make_maps(&maps, p, PvF16)) return cudaErrorInvalidValue;
   const DeviceInfo& di = device_info();
   const uint64_t bit = 1ull << (di.device & 63);
   if ((configured.load() & bit) == 0) {
     const cudaError_t e =
-        cudaFuncSetAttribute(decode_partial_mma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(decode_partial_mma_kernel<D, PvF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
@@ -807,8 +819,8 @@ cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t strea
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
-  return launch_pdl(decode_partial_mma_kernel<D>, static_cast<unsigned>(grid), kMmaThreads, C::kSmem, stream, p,
-                    maps);
+  return launch_pdl(decode_partial_mma_kernel<D, PvF16>, static_cast<unsigned>(grid), kMmaThreads, C::kSmem,
+                    stream, p, maps);
 }
 
 }  // namespace
@@ -821,8 +833,8 @@ bool mma_path_applies(const DecodeParams& p, int q_dtype, int pool_dtype) {
 }
 
 cudaError_t decode_dispatch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
-  if (p.d == 128) return launch_mma<128>(p, grid_limit, stream);
-  return launch_mma<256>(p, grid_limit, stream);
+  if (p.d == 128) return launch_mma<128, false>(p, grid_limit, stream);
+  return launch_mma<256, false>(p, grid_limit, stream);
 }
 
 // ---- fp8 pools: bf16 copies of the sequences for the tensor-core kernel
@@ -832,7 +844,8 @@ constexpr int kWidenThreads = 256;
 
 // One CTA per (sequence b, 64-position page t of the copies, KV head h): the E4M3 codes of K and V
 // at positions 64t .. 64t + 63 (up to the sequence's length), read through the block table and
-// written as bf16 into the copies -- exactly, since every E4M3 value is a bf16 value. The page's
+// written into the copies, K as bf16 and V as f16 -- exactly, since every E4M3 value (3 mantissa
+// bits, magnitudes 2^-9 .. 448) is both a bf16 and an f16 value. The page's
 // table entry is its own index, or -1 when the source page id is outside the pool (its positions
 // then stay masked, as the SIMT kernel skips them). Pages past the length are not touched.
 __global__ void __launch_bounds__(kWidenThreads) widen_kernel(DecodeParams p) {
@@ -867,10 +880,17 @@ __global__ void __launch_bounds__(kWidenThreads) widen_kernel(DecodeParams p) {
       for (int i = 0; i < 4; ++i) {
         const float2 lo = e4m3x2_to_float2(w[i] & 0xffffu);
         const float2 hi = e4m3x2_to_float2(w[i] >> 16);
-        const __nv_bfloat162 a = __floats2bfloat162_rn(lo.x, lo.y);
-        const __nv_bfloat162 bb = __floats2bfloat162_rn(hi.x, hi.y);
-        o[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
-        o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+        if (kv == 0) {   // K: bf16, the format of Q in QK^T
+          const __nv_bfloat162 a = __floats2bfloat162_rn(lo.x, lo.y);
+          const __nv_bfloat162 bb = __floats2bfloat162_rn(hi.x, hi.y);
+          o[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
+          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+        } else {         // V: f16, so P can enter PV as one f16 term
+          const __half2 a = __floats2half2_rn(lo.x, lo.y);
+          const __half2 bb = __floats2half2_rn(hi.x, hi.y);
+          o[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
+          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bb);
+        }
       }
       dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
       dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -897,7 +917,8 @@ cudaError_t decode_dispatch_widened(const DecodeParams& p, int grid_limit, cudaS
   w.max_pages = p.t64;
   w.page_tokens = kMmaN;
   w.num_pages = p.batch * p.t64;
-  return decode_dispatch_mma(w, grid_limit, stream);
+  if (w.d == 128) return launch_mma<128, true>(w, grid_limit, stream);
+  return launch_mma<256, true>(w, grid_limit, stream);
 }
 
 
