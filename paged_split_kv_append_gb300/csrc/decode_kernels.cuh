@@ -71,6 +71,9 @@ struct DecodeCfg {
   // the epilogue's cross-warp scratch lives in the unit's last stage when a stage can hold it (every
   // format but E4M3), which leaves room for one more stage
   static constexpr bool kRedInStage = kStageBytes >= kRedFloats * 4;
+  // small page tiles (4 KB or less) are moved by the producer warp's 32 lanes with 16-byte cp.async
+  // copies: the copy engine's fixed cost per bulk request would cap the stream below HBM speed
+  static constexpr bool kWarpCopy = kTileBytes <= 4096;
   static constexpr int kFixed = 2 * kQBytes + (kRedInStage ? 0 : 2 * kRedFloats * 4) + kPBufBytes +
                                 2 * (int)sizeof(UnitMeta) + 2048;
   // resident CTAs per SM: 3 (2 at head dim 256, where the registers allow no more), fewer when
@@ -215,7 +218,9 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&sm.full[i], 1);
+      // bulk copies: lane 0's arrive with the byte count; warp copies: each lane's cp.async
+      // completion plus lane 0's arrive after it published the stage's tile bits
+      mbar_init(&sm.full[i], C::kWarpCopy ? 33 : 1);
       mbar_init(&sm.empty[i], NW);
     }
     for (int i = 0; i < 2; ++i) {
@@ -309,12 +314,12 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
           }
           pages[hf] = __shfl_sync(0xffffffffu, my_page, (pi - pc) & 31);
         }
+        const uint32_t stage = tile_seq % NS;
+        int okbits = 0;
         if (lane == 0) {
-          const uint32_t stage = tile_seq % NS;
           if (tile_seq >= static_cast<uint32_t>(NS))
             ok = wait_or_abort(&sm.empty[stage], ((tile_seq / NS) - 1) & 1u, abort_flag);
           if (ok) {
-            int okbits = 0;
             uint32_t bytes = 0;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -329,7 +334,9 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
             }
             sm.stage_ok[stage] = okbits;
             char* dst = sm.stages + stage * C::kStageBytes;
-            if (bytes) {
+            if (C::kWarpCopy) {
+              mbar_arrive(&sm.full[stage]);   // releases the tile bits; the lanes' copies follow
+            } else if (bytes) {
               mbar_arrive_expect_tx(&sm.full[stage], bytes);
 #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
@@ -350,11 +357,32 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) break;
+        if constexpr (C::kWarpCopy) {
+          // the stage's tiles in 16-byte pieces, 512 contiguous bytes per warp instruction
+          okbits = __shfl_sync(0xffffffffu, okbits, 0);
+          const uint32_t dst = smem_u32(sm.stages + stage * C::kStageBytes);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!((okbits >> hf) & 1)) continue;
+            const int nh = n0 + hf * kTileN;
+            const int64_t off =
+                ((static_cast<int64_t>(pages[hf]) * p.h_kv + h) * P + (nh - (nh / P) * P)) * D * PT::kBytes;
+            const char* ks = static_cast<const char*>(p.k_pool) + off;
+            const char* vs = static_cast<const char*>(p.v_pool) + off;
+#pragma unroll
+            for (int c = lane; c < C::kTileBytes / 16; c += 32) {
+              cp_async16(dst + hf * C::kTileBytes + c * 16, ks + c * 16);
+              cp_async16(dst + C::kHalfBytes + hf * C::kTileBytes + c * 16, vs + c * 16);
+            }
+          }
+          cp_async_arrive_noinc(&sm.full[stage]);
+        }
         ++tile_seq;
       }
       ++unit_seq;
       u = __shfl_sync(0xffffffffu, u_next, 0);
     }
+    if constexpr (C::kWarpCopy) cp_async_wait_all();   // this lane's copies have landed
     if (!ok && lane == 0) {
       // gave up: record it, then let the copies already issued land before the CTA exits
       raise_status(p.status, NBX_DEV_TIMEOUT);

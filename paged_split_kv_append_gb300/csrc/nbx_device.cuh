@@ -257,6 +257,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// 16-byte asynchronous copy global -> shared through L2 only (cp.async.cg; both addresses 16-byte
+// aligned), tracked per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src_gmem) : "memory");
+}
+// Arrives on `bar` once every cp.async this thread issued before has completed; the arrival is one
+// of the barrier's expected arrivals (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Waits for every cp.async this thread issued.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Orders this thread's generic-proxy shared-memory accesses before later async-proxy accesses (bulk
 // copies) of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
