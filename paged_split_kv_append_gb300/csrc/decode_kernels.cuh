@@ -68,9 +68,10 @@ struct DecodeCfg {
   static constexpr int kQBytes = kQB * D * QT::kBytes;
   static constexpr int kRedFloats = kConsumerWarps * (kQB * D + 2 * kQB);   // one slot
   static constexpr int kPBufBytes = kConsumerWarps * kPassTok * kQB * 8;      // (p, p) pairs
-  // the epilogue's cross-warp scratch lives in the unit's last stage when a stage can hold it (every
-  // format but E4M3), which leaves room for one more stage
-  static constexpr bool kRedInStage = kStageBytes >= kRedFloats * 4;
+  // the epilogue's cross-warp scratch lives in the unit's last stage when each warp's own K rows of
+  // it hold the warp's accumulators (pool elements of 2 bytes or more), which leaves room for one
+  // more stage; a warp reads only its own positions' rows, so it may write over them at once
+  static constexpr bool kRedInStage = kWarpTok * D * PT::kBytes >= kQB * D * 4;
   // small page tiles (4 KB or less) are moved by the producer warp's 32 lanes with 16-byte cp.async
   // copies: the copy engine's fixed cost per bulk request would cap the stream below HBM speed
   static constexpr bool kWarpCopy = kTileBytes <= 4096;
@@ -85,6 +86,7 @@ struct DecodeCfg {
   static constexpr int kStagesRaw = (kSmemPerCta - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : (kStagesRaw < 2 ? 2 : kStagesRaw);
   static_assert(kWarpTok % kPassTok == 0, "a warp's share of a stage holds whole passes");
+  static_assert(!kRedInStage || kWarpTok * D * PT::kBytes >= 2 * kQB * 4, "a warp's V rows hold its m and l");
   static_assert(kLPT >= 4 && kLPT <= 16, "head dim 64..256");
 };
 
@@ -576,28 +578,30 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
     }
     if (!ok) break;
 
-    // ---- epilogue: merge the four warps' states in warp order, through the unit's last stage (its
-    // K/V are consumed) or a double-buffered scratch
-    float* red;
-    if constexpr (C::kRedInStage) {
-      // every warp has finished reading the stage before any warp writes its state over it
-      if (!csync()) {
-        ok = false;
-        break;
-      }
-      red = reinterpret_cast<float*>(sm.stages + last_stage * C::kStageBytes);
-    } else {
-      red = sm.red + slot * C::kRedFloats;
-    }
+    // ---- epilogue: merge the four warps' states in warp order. Warp w's state (acc [kQB][D], then
+    // m [kQB] and l [kQB]) sits over its own K rows and V rows of the unit's last stage, which only
+    // it reads, or in a double-buffered scratch.
+    char* const red_base = C::kRedInStage ? sm.stages + last_stage * C::kStageBytes
+                                          : reinterpret_cast<char*>(sm.red + slot * C::kRedFloats);
+    auto acc_of = [&](int w) -> float* {
+      return C::kRedInStage ? reinterpret_cast<float*>(red_base + w * C::kWarpTok * D * PT::kBytes)
+                            : reinterpret_cast<float*>(red_base) + w * (kQB * D + 2 * kQB);
+    };
+    auto ml_of = [&](int w) -> float* {
+      return C::kRedInStage ? reinterpret_cast<float*>(red_base + C::kHalfBytes + w * C::kWarpTok * D * PT::kBytes)
+                            : reinterpret_cast<float*>(red_base) + w * (kQB * D + 2 * kQB) + kQB * D;
+    };
     {
       float l_tot = l_run;
       if constexpr (TPG == 2) l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 1);
 #pragma unroll
       for (int off = LPT; off < 32; off <<= 1) l_tot += __shfl_xor_sync(0xffffffffu, l_tot, off);
-      float* rw = red + warp * (kQB * D + 2 * kQB);
+      __syncwarp();   // every lane of this warp is done with its rows of the last stage
+      float* rw = acc_of(warp);
+      float* rm = ml_of(warp);
       if (lane < 8 && tsel == 0) {   // one lane per vector
-        rw[kQB * D + vsel] = m_run;
-        rw[kQB * D + kQB + vsel] = l_tot;
+        rm[vsel] = m_run;
+        rm[kQB + vsel] = l_tot;
       }
 #pragma unroll
       for (int i = 0; i < kQB; ++i)
@@ -618,17 +622,16 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
       if (i >= u_nvec) continue;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = max_nan(M, red[w * (kQB * D + 2 * kQB) + kQB * D + i]);
+      for (int w = 0; w < NW; ++w) M = max_nan(M, ml_of(w)[i]);
       float L = 0.f, A = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-          const float* rw = red + w * (kQB * D + 2 * kQB);
-          const float mw = rw[kQB * D + i];
+          const float mw = ml_of(w)[i];
           if (mw != -INFINITY) {
             const float f = fast_exp2(mw - M);
-            L += f * rw[kQB * D + kQB + i];
-            A += f * rw[i * D + dd];
+            L += f * ml_of(w)[kQB + i];
+            A += f * acc_of(w)[i * D + dd];
           }
         }
       }
