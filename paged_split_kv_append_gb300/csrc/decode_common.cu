@@ -94,12 +94,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
     const int align = p.page_tokens <= NBX_SPLIT_POSITIONS ? p.page_tokens : NBX_SPLIT_POSITIONS;
     seg = ((seg + align - 1) / align) * align;
     const int n = L > 0 ? (L + seg - 1) / seg : 0;
-    SeqPlan sp;
-    sp.len = L;
-    sp.seg = seg;
-    sp.n_splits = n;
-    sp.pad = 0;
-    p.plan[b] = sp;
+    // kept in L2 for the merge, which reads the split counts after the K/V stream
+    st_global_hint(reinterpret_cast<int4*>(p.plan + b), make_int4(L, seg, n, 0), l2_evict_last_policy());
     if (n == 0) s_empty = 1;
     if (small) {
       s_len[b] = L;
@@ -272,6 +268,30 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
     const int nvec = min(kQB, RG - q0);
     const int S = p.plan[b].n_splits;
     if (S <= 1) continue;   // one split: the partial kernel wrote the output
+    // Each thread owns float4 outputs o = tid, tid + 128, ...: output o is element 4 * (o % d4) of
+    // vector o / d4. The partial accumulators need only S, so the first batch of the first output
+    // is loaded before the weights are computed and waits beside the m / l loads.
+    const int d4 = p.d / 4;
+    const int n_out = nvec * d4;
+    auto acc_row = [&](int o, int& i, int& dd, long long& orow) {
+      i = o / d4;
+      dd = (o - i * d4) * 4;
+      const int qi = q0 + i;
+      const int r = qi / p.group;
+      const int g = qi - r * p.group;
+      orow = (static_cast<long long>(b) * p.rows + r) * p.h_q + static_cast<long long>(h) * p.group + g;
+    };
+    auto load_batch = [&](int o, int s0, float4 (&a)[32]) {
+      int i, dd;
+      long long orow;
+      acc_row(o, i, dd, orow);
+      const float4* acc = reinterpret_cast<const float4*>(p.acc_part + orow * p.max_splits * p.d + dd);
+#pragma unroll
+      for (int k = 0; k < 32; ++k)
+        a[k] = (s0 + k < S) ? acc[static_cast<long long>(s0 + k) * d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    float4 a[32];
+    if (tid < n_out) load_batch(tid, 0, a);
     // warp i: vector i's split weights. Lanes hold splits lane and lane + 32; max and sums are
     // butterfly reductions, a fixed order.
     if (warp < nvec) {
@@ -308,23 +328,14 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
       }
     }
     __syncthreads();
-    // each thread a float4 of one vector's output, every split's load in flight, summed in
-    // ascending split order
-    const int d4 = p.d / 4;
-    for (int o = tid; o < nvec * d4; o += kDecodeMergeThreads) {
-      const int i = o / d4;
-      const int dd = (o - i * d4) * 4;
-      const int qi = q0 + i;
-      const int r = qi / p.group;
-      const int g = qi - r * p.group;
-      const long long orow = (static_cast<long long>(b) * p.rows + r) * p.h_q + static_cast<long long>(h) * p.group + g;
-      const float4* acc = reinterpret_cast<const float4*>(p.acc_part + orow * p.max_splits * p.d + dd);
+    // every split's weighted accumulator summed in ascending split order
+    for (int o = tid; o < n_out; o += kDecodeMergeThreads) {
+      int i, dd;
+      long long orow;
+      acc_row(o, i, dd, orow);
       float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int s0 = 0; s0 < S; s0 += 32) {
-        float4 a[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          a[k] = (s0 + k < S) ? acc[static_cast<long long>(s0 + k) * d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0 > 0) load_batch(o, s0, a);
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           if (s0 + k >= S) break;
@@ -340,6 +351,7 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
       const float sc = s_scale[i];
       const float4 res = s_dead[i] ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A.x * sc, A.y * sc, A.z * sc, A.w * sc);
       *reinterpret_cast<float4*>(p.out + orow * p.d + dd) = res;
+      if (o + kDecodeMergeThreads < n_out) load_batch(o + kDecodeMergeThreads, 0, a);
     }
     __syncthreads();
   }

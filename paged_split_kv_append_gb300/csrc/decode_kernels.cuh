@@ -266,8 +266,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
       const int rem = u - e_idx * unit_span;
       const int h = rem / p.row_blocks;
       const int rb = rem - h * p.row_blocks;
-      const Entry en = p.entries[e_idx];
-      const SeqPlan sp = p.plan[en.b];
+      const Entry en = p.entries[e_idx];   // carries its sequence's length and split count
       int u_next = 0;
       if (lane == 0) u_next = atomicAdd(&p.header[1], 1);
       if (lane == 0) {
@@ -277,7 +276,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
         mt.h = h;
         mt.start = en.start;
         mt.end = en.end;
-        mt.n_splits = sp.n_splits;
+        mt.n_splits = en.n_splits;
         const int q0 = rb * kQB;
         const int nvalid = min(kQB, RG - q0);
         mt.nvec = nvalid;
@@ -288,7 +287,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
           const int r = qi / p.group;
           const int g = qi - r * p.group;
           const bool vq = i < nvalid;
-          mt.pos[i] = vq ? sp.len - p.rows + r : -1;
+          mt.pos[i] = vq ? en.len - p.rows + r : -1;
           mt.orow[i] = vq ? (static_cast<int64_t>(en.b) * p.rows + r) * p.h_q + static_cast<int64_t>(h) * p.group + g
                           : 0;
         }
@@ -614,12 +613,17 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
     }
     const bool multi = mtp->n_splits > 1;
     const int u_split = mtp->s;
+    // the merged values go to registers first: the last stage and the metadata slot are handed back
+    // before the global stores, so neither the proxy fence nor the arrives wait behind them
+    constexpr int kOut = kQB * D / (NW * 32);
+    float r_a[kOut], r_m[kOut], r_l[kOut];
+    int64_t r_row[kOut];
 #pragma unroll
-    for (int x = 0; x < kQB * D / (NW * 32); ++x) {
+    for (int x = 0; x < kOut; ++x) {
       const int o = ct + x * NW * 32;
       const int i = o / D;
       const int dd = o - i * D;
-      if (i >= u_nvec) continue;
+      r_row[x] = i < u_nvec ? mtp->orow[i] : -1;
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NW; ++w) M = max_nan(M, ml_of(w)[i]);
@@ -635,26 +639,36 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
           }
         }
       }
-      const int64_t orow = mtp->orow[i];
-      if (!multi) {
-        p.out[orow * D + dd] = (M == -INFINITY) ? 0.f : A * (p.v_scale / L);
-      } else {
-        const int64_t prow = orow * p.max_splits + u_split;
-        p.acc_part[prow * D + dd] = A;
-        if (dd == 0) {
-          p.m_part[prow] = M;
-          p.l_part[prow] = L;
-        }
-      }
+      r_a[x] = A;
+      r_m[x] = M;
+      r_l[x] = L;
     }
     if constexpr (C::kRedInStage) {
-      // the stage goes back to the producer: these generic writes come before its next bulk copy
-      fence_proxy_async_smem();
+      // the stage goes back to the producer. Its next fill is a bulk copy (async proxy) unless the
+      // tiles are warp copies: cp.async is a generic-proxy write, ordered by the barrier alone.
+      if constexpr (!C::kWarpCopy) fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[last_stage]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.qempty[slot]);   // the slot's queries and metadata are free again
+#pragma unroll
+    for (int x = 0; x < kOut; ++x) {
+      if (r_row[x] < 0) continue;
+      const int dd = (ct + x * NW * 32) % D;
+      if (!multi) {
+        p.out[r_row[x] * D + dd] = (r_m[x] == -INFINITY) ? 0.f : r_a[x] * (p.v_scale / r_l[x]);
+      } else {
+        // the partial stays in L2 for the merge
+        const uint64_t keep = l2_evict_last_policy();
+        const int64_t prow = r_row[x] * p.max_splits + u_split;
+        st_global_hint(p.acc_part + prow * D + dd, r_a[x], keep);
+        if (dd == 0) {
+          st_global_hint(p.m_part + prow, r_m[x], keep);
+          st_global_hint(p.l_part + prow, r_l[x], keep);
+        }
+      }
+    }
     ++unit_seq;
   }
 
