@@ -243,103 +243,86 @@ cudaError_t merge_dispatch(const MergeParams& p, cudaStream_t stream) {
 }
 
 // ------------------------------------------------------------------------------------ decode merge
-constexpr int kDecodeMergeThreads = 128;
+constexpr int kDecodeMergeThreads = 32;   // one warp per CTA
 
-// Merges the split partials of every (sequence, KV head, row block) with more than one split:
-// M = max_s m_s, w_s = 2^(m_s - M) (m in log2 units; splits with m = -inf skipped),
+// Merges the split partials of every query vector of a (sequence, KV head) with more than one
+// split: M = max_s m_s, w_s = 2^(m_s - M) (m in log2 units; splits with m = -inf skipped),
 // out = v_scale * sum_s w_s acc_s / sum_s w_s l_s, s ascending. One-split sequences were written
 // by the partial kernel.
+// One warp per query vector, each its own CTA so the work spreads evenly over the SMs: lane k holds
+// m and l of splits k and k + 32 (max and sums are butterfly reductions, a fixed order), the
+// weights reach every lane by shuffles, and each lane owns float4 pieces of the output, with every
+// split's accumulator load in flight and the sum in ascending split order.
 __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(DecodeParams p) {
-  __shared__ float s_w[kQB][NBX_MAX_SPLITS];   // weight of each live split, -1 for a split with no visible key
-  __shared__ float s_scale[kQB];
-  __shared__ int s_dead[kQB];
-  pdl_wait();   // every partial of the decode is written and visible from here on
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
+  const int lane = threadIdx.x;
   const int RG = p.rows * p.group;
   const int per_seq = p.h_kv * p.row_blocks;
-  const int n_groups = p.batch * per_seq;
-  for (int gi = blockIdx.x; gi < n_groups; gi += gridDim.x) {
-    const int b = gi / per_seq;
-    const int rem = gi - b * per_seq;
+  const int64_t n_items = static_cast<int64_t>(p.batch) * per_seq * kQB;
+  // The plan kernel had completed before any CTA of the partial kernel passed its own wait, and this
+  // grid is launched only after they did, so the first item's split count can be read (from L2)
+  // before this grid waits for the partials.
+  int s_first = 0;
+  if (blockIdx.x < n_items) s_first = __ldcg(&p.plan[blockIdx.x / (static_cast<int64_t>(per_seq) * kQB)].n_splits);
+  pdl_wait();   // every partial of the decode is written and visible from here on
+  const int d4 = p.d / 4;
+  for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int64_t gi = it / kQB;
+    const int i = static_cast<int>(it - gi * kQB);
+    const int b = static_cast<int>(gi / per_seq);
+    const int rem = static_cast<int>(gi - static_cast<int64_t>(b) * per_seq);
     const int h = rem / p.row_blocks;
     const int rb = rem - h * p.row_blocks;
-    const int q0 = rb * kQB;
-    const int nvec = min(kQB, RG - q0);
-    const int S = p.plan[b].n_splits;
-    if (S <= 1) continue;   // one split: the partial kernel wrote the output
-    // Each thread owns float4 outputs o = tid, tid + 128, ...: output o is element 4 * (o % d4) of
-    // vector o / d4. The partial accumulators need only S, so the first batch of the first output
-    // is loaded before the weights are computed and waits beside the m / l loads.
-    const int d4 = p.d / 4;
-    const int n_out = nvec * d4;
-    auto acc_row = [&](int o, int& i, int& dd, long long& orow) {
-      i = o / d4;
-      dd = (o - i * d4) * 4;
-      const int qi = q0 + i;
-      const int r = qi / p.group;
-      const int g = qi - r * p.group;
-      orow = (static_cast<long long>(b) * p.rows + r) * p.h_q + static_cast<long long>(h) * p.group + g;
-    };
-    auto load_batch = [&](int o, int s0, float4 (&a)[32]) {
-      int i, dd;
-      long long orow;
-      acc_row(o, i, dd, orow);
-      const float4* acc = reinterpret_cast<const float4*>(p.acc_part + orow * p.max_splits * p.d + dd);
+    const int qi = rb * kQB + i;
+    if (qi >= RG) continue;
+    const int S = it == blockIdx.x ? s_first : p.plan[b].n_splits;
+    if (S <= 1) continue;
+    const int r = qi / p.group;
+    const int g = qi - r * p.group;
+    const int64_t orow = (static_cast<int64_t>(b) * p.rows + r) * p.h_q + static_cast<int64_t>(h) * p.group + g;
+    const float* m = p.m_part + orow * p.max_splits;
+    const float* l = p.l_part + orow * p.max_splits;
+    const float4* acc = reinterpret_cast<const float4*>(p.acc_part + orow * p.max_splits * p.d);
+    auto load_batch = [&](int j, int s0, float4 (&a)[32]) {
 #pragma unroll
       for (int k = 0; k < 32; ++k)
-        a[k] = (s0 + k < S) ? acc[static_cast<long long>(s0 + k) * d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[k] = (j < d4 && s0 + k < S) ? acc[static_cast<int64_t>(s0 + k) * d4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     float4 a[32];
-    if (tid < n_out) load_batch(tid, 0, a);
-    // warp i: vector i's split weights. Lanes hold splits lane and lane + 32; max and sums are
-    // butterfly reductions, a fixed order.
-    if (warp < nvec) {
-      const int qi = q0 + warp;
-      const int r = qi / p.group;
-      const int g = qi - r * p.group;
-      const long long orow = (static_cast<long long>(b) * p.rows + r) * p.h_q + static_cast<long long>(h) * p.group + g;
-      const float* m = p.m_part + orow * p.max_splits;
-      const float* l = p.l_part + orow * p.max_splits;
-      float mv[2], lv[2];
-      bool live[2];
+    load_batch(lane, 0, a);   // in flight together with the m / l loads
+    float mv[2], lv[2];
+    bool live[2];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int sp = lane + 32 * k;
-        mv[k] = sp < S ? m[sp] : -INFINITY;
-        lv[k] = sp < S ? l[sp] : 0.f;
-        live[k] = mv[k] != -INFINITY;
-      }
-      float M = max_nan(mv[0], mv[1]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
-      float L = 0.f;
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const float w = live[k] ? fast_exp2(mv[k] - M) : 0.f;
-        if (live[k]) L += w * lv[k];
-        if (lane + 32 * k < NBX_MAX_SPLITS) s_w[warp][lane + 32 * k] = live[k] ? w : -1.f;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-      if (lane == 0) {
-        s_dead[warp] = (M == -INFINITY) ? 1 : 0;
-        s_scale[warp] = p.v_scale / L;
-      }
+    for (int k = 0; k < 2; ++k) {
+      const int sp = lane + 32 * k;
+      mv[k] = sp < S ? m[sp] : -INFINITY;
+      lv[k] = sp < S ? l[sp] : 0.f;
+      live[k] = mv[k] != -INFINITY;
     }
-    __syncthreads();
-    // every split's weighted accumulator summed in ascending split order
-    for (int o = tid; o < n_out; o += kDecodeMergeThreads) {
-      int i, dd;
-      long long orow;
-      acc_row(o, i, dd, orow);
+    float M = max_nan(mv[0], mv[1]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float L = 0.f;
+    float wv[2];   // weight of split lane + 32k, -1 for a split with no visible key
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float w = live[k] ? fast_exp2(mv[k] - M) : 0.f;
+      if (live[k]) L += w * lv[k];
+      wv[k] = live[k] ? w : -1.f;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    const bool dead = M == -INFINITY;
+    const float sc = p.v_scale / L;
+    for (int j0 = 0; j0 < d4; j0 += 32) {   // every lane runs every pass: the shuffles need the whole warp
+      const int j = j0 + lane;
       float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int s0 = 0; s0 < S; s0 += 32) {
-        if (s0 > 0) load_batch(o, s0, a);
+        if (j0 > 0 || s0 > 0) load_batch(j, s0, a);
+        const float wsrc = s0 == 0 ? wv[0] : wv[1];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           if (s0 + k >= S) break;
-          const float w = s_w[i][s0 + k];
+          const float w = __shfl_sync(0xffffffffu, wsrc, k);
           if (w != -1.f) {
             A.x += w * a[k].x;
             A.y += w * a[k].y;
@@ -348,12 +331,10 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
           }
         }
       }
-      const float sc = s_scale[i];
-      const float4 res = s_dead[i] ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A.x * sc, A.y * sc, A.z * sc, A.w * sc);
-      *reinterpret_cast<float4*>(p.out + orow * p.d + dd) = res;
-      if (o + kDecodeMergeThreads < n_out) load_batch(o + kDecodeMergeThreads, 0, a);
+      if (j < d4)
+        reinterpret_cast<float4*>(p.out + orow * p.d)[j] =
+            dead ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A.x * sc, A.y * sc, A.z * sc, A.w * sc);
     }
-    __syncthreads();
   }
 }
 
@@ -369,9 +350,9 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
   else e = decode_dispatch_E4M3(p, q_dtype, grid_limit, stream);
   if (e != cudaSuccess) return e;
   if (p.max_splits <= 1) return cudaSuccess;   // every sequence has one split: the partials are the output
-  const int64_t groups = static_cast<int64_t>(p.batch) * p.h_kv * p.row_blocks;
-  int64_t grid = static_cast<int64_t>(device_info().sm_count) * 4;
-  if (grid > groups) grid = groups;
+  const int64_t items = static_cast<int64_t>(p.batch) * p.h_kv * p.row_blocks * kQB;
+  int64_t grid = static_cast<int64_t>(device_info().sm_count) * 16;
+  if (grid > items) grid = items;
   return launch_pdl(decode_merge_kernel, static_cast<unsigned>(grid), kDecodeMergeThreads, 0, stream, p);
 }
 
