@@ -208,6 +208,10 @@ static int decode_call(const void* q, int q_dtype, int batch, int rows, int h_q,
   p.widen_v = widen ? ws + w.widen_v : nullptr;
   p.widen_bt = widen ? reinterpret_cast<int32_t*>(ws + w.widen_bt) : nullptr;
   p.t64 = w.t64;
+  {
+    const double part_bytes = static_cast<double>(batch) * rows * h_q * w.max_splits * d * 4.0;
+    p.keep_frac = static_cast<float>(part_bytes <= 67108864.0 ? 1.0 : 67108864.0 / part_bytes);
+  }
   const cudaError_t e = decode_dispatch(p, q_dtype, pool_dtype, g_grid_limit.load(), stream);
   return e == cudaSuccess ? NBX_OK : NBX_ERR_CUDA;
 }

@@ -660,7 +660,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
         p.out[r_row[x] * D + dd] = (r_m[x] == -INFINITY) ? 0.f : r_a[x] * (p.v_scale / r_l[x]);
       } else {
         // the partial stays in L2 for the merge
-        const uint64_t keep = l2_evict_last_policy();
+        const uint64_t keep = l2_keep_policy(p.keep_frac);
         const int64_t prow = r_row[x] * p.max_splits + u_split;
         st_global_hint(p.acc_part + prow * D + dd, r_a[x], keep);
         if (dd == 0) {

@@ -172,6 +172,13 @@ __device__ __forceinline__ void st_global_v8(float* dst, const float (&v)[8]) {
                : "memory");
 }
 
+// The same, with an L2 cache policy.
+__device__ __forceinline__ void st_global_v8_hint(float* dst, const float (&v)[8], uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(dst), "f"(v[0]),
+               "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "l"(pol)
+               : "memory");
+}
+
 // Shared-memory matrix descriptor: start >> 4 in bits [0,14), leading byte offset >> 4 in [16,30),
 // stride byte offset >> 4 in [32,46), descriptor version 1 in [46,48), base offset 0 (operand
 // blocks are 1024-byte aligned), layout 2 = 128-byte swizzle in [61,64).
@@ -578,6 +585,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int rt = row / G;                       // query row within the M tile
     const int gq = row - rt * G;                  // query head within the KV head's group
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // the split partials stay in L2 for the merge
+    const uint64_t keep = l2_keep_policy(p.keep_frac);
     bool ok = true;
     uint32_t g = 0;              // tile ordinal
     uint32_t gb = 0, gp = 0;     // S/P buffer (g % 3) and its phase count (g / 3)
@@ -714,8 +723,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         const int64_t orow = (static_cast<int64_t>(mu.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mu.h) * G + gq;
         dst = single ? p.out + orow * D : p.acc_part + (orow * p.max_splits + mu.s) * D;
         if (!single) {
-          p.m_part[orow * p.max_splits + mu.s] = m_run;
-          p.l_part[orow * p.max_splits + mu.s] = l_run;
+          st_global_hint(p.m_part + orow * p.max_splits + mu.s, m_run, keep);
+          st_global_hint(p.l_part + orow * p.max_splits + mu.s, l_run, keep);
         }
       }
 #pragma unroll 1
@@ -734,7 +743,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             float v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(ov[8 * c8 + e]) * sc;
-            st_global_v8(dst + ch * kChunk + c8 * 8, v);
+            if (single) st_global_v8(dst + ch * kChunk + c8 * 8, v);
+            else st_global_v8_hint(dst + ch * kChunk + c8 * 8, v, keep);   // kept in L2 for the merge
           }
         }
       }

@@ -311,6 +311,12 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// The same, applied to the given fraction (0, 1] of the lines written.
+__device__ __forceinline__ uint64_t l2_keep_policy(float frac) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, %1;" : "=l"(pol) : "f"(frac));
+  return pol;
+}
 __device__ __forceinline__ void st_global_hint(float* dst, float v, uint64_t pol) {
   asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(dst), "f"(v), "l"(pol) : "memory");
 }

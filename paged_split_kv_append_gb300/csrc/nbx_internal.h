@@ -115,6 +115,9 @@ struct DecodeParams {
   int32_t* ident_bt;
   int32_t* lens_out;
   int len_add;
+  // fraction of the split partials' lines written with an L2 evict-last policy: about 64 MB of them
+  // stay resident for the merge (1 when they all fit)
+  float keep_frac;
 };
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);
