@@ -436,18 +436,18 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
     // ---- query vectors: this lane's 16 elements of each, scaled into log2 units
     f32x2 q2[kQB][8];
     {
-      const char* qs = sm.qbuf + slot * C::kQBytes;
+      // the lane's elements of a vector come in runs of EPV, one wide shared load each
+      const uint32_t qs = smem_u32(sm.qbuf + slot * C::kQBytes);
+      const f32x2 sc2 = pack2(p.qk_scale_log2, p.qk_scale_log2);
 #pragma unroll
       for (int i = 0; i < kQB; ++i) {
         const bool vq = i < u_nvec;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
+          f32x2 x[EPV / 2];
+          lds_row_x2<QT, EPV>(qs + static_cast<uint32_t>((i * D + (j + v * LPT) * EPV) * QT::kBytes), x);
 #pragma unroll
-          for (int e2 = 0; e2 < EPV / 2; ++e2) {
-            const int el = (j + v * LPT) * EPV + 2 * e2;
-            const float2 x = load_pair<QT>(qs + (i * D + el) * QT::kBytes);
-            q2[i][v * (EPV / 2) + e2] = vq ? pack2(x.x * p.qk_scale_log2, x.y * p.qk_scale_log2) : 0ull;
-          }
+          for (int e2 = 0; e2 < EPV / 2; ++e2) q2[i][v * (EPV / 2) + e2] = vq ? mul2(x[e2], sc2) : 0ull;
         }
       }
     }
