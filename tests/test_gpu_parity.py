@@ -96,6 +96,19 @@ def test_decode_edge_lengths(lens):
     assert np.all(out.cpu().numpy()[np.array(lens) == 0] == 0.0)
 
 
+@pytest.mark.parametrize("batch,hi", [(100, 900), (2100, 40)])
+def test_decode_plan_paths_by_batch_size(batch, hi):
+    # up to 2048 sequences are planned by the block-wide sort, more by the serial path; lengths of
+    # 0 cover each path's empty sequences (output rows written as 0)
+    cfg = wl.Config("plan_b%d" % batch, batch, 1, 4, 2, 64, 16, "bf16", "bf16", 31, ("uniform", 0, hi))
+    lens = np.random.default_rng(batch).integers(0, hi + 1, batch)
+    lens[::7] = 0
+    case = wl.make_case(cfg, device=DEV, lens=[int(x) for x in lens])
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+    assert np.all(out.cpu().numpy()[case.lens == 0] == 0.0)
+
+
 def test_decode_multi_row_short_sequences():
     # rows > length (some rows see no key), lengths ending mid-page, GQA group 3, fp32 queries
     cfg = wl.Config("mr", 5, 5, 6, 2, 64, 16, "bf16", "f32", 21, ("fixed", (3, 17, 1, 0, 40)))
