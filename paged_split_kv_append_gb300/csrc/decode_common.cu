@@ -249,25 +249,30 @@ constexpr int kDecodeMergeThreads = 32;   // one warp per CTA
 // split: M = max_s m_s, w_s = 2^(m_s - M) (m in log2 units; splits with m = -inf skipped),
 // out = v_scale * sum_s w_s acc_s / sum_s w_s l_s, s ascending. One-split sequences were written
 // by the partial kernel.
-// One warp per query vector, each its own CTA so the work spreads evenly over the SMs: lane k holds
-// m and l of splits k and k + 32 (max and sums are butterfly reductions, a fixed order), the
-// weights reach every lane by shuffles, and each lane owns float4 pieces of the output, with every
-// split's accumulator load in flight and the sum in ascending split order.
+// One warp per query vector and 128 output columns, each its own CTA so the work spreads evenly
+// over the SMs: lane k holds m and l of splits k and k + 32 (max and sums are butterfly
+// reductions, a fixed order), the weights reach every lane by shuffles, and each lane owns one
+// float4 of the output, with every split's accumulator load in flight and the sum in ascending
+// split order.
 __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(DecodeParams p) {
   const int lane = threadIdx.x;
   const int RG = p.rows * p.group;
   const int per_seq = p.h_kv * p.row_blocks;
-  const int64_t n_items = static_cast<int64_t>(p.batch) * per_seq * kQB;
+  const int d4 = p.d / 4;
+  const int n_col = (d4 + 31) / 32;   // 128-column pieces of a vector
+  const int64_t n_items = static_cast<int64_t>(p.batch) * per_seq * kQB * n_col;
   // The plan kernel had completed before any CTA of the partial kernel passed its own wait, and this
   // grid is launched only after they did, so the first item's split count can be read (from L2)
   // before this grid waits for the partials.
   int s_first = 0;
-  if (blockIdx.x < n_items) s_first = __ldcg(&p.plan[blockIdx.x / (static_cast<int64_t>(per_seq) * kQB)].n_splits);
+  if (blockIdx.x < n_items)
+    s_first = __ldcg(&p.plan[blockIdx.x / (static_cast<int64_t>(per_seq) * kQB * n_col)].n_splits);
   pdl_wait();   // every partial of the decode is written and visible from here on
-  const int d4 = p.d / 4;
   for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int64_t gi = it / kQB;
-    const int i = static_cast<int>(it - gi * kQB);
+    const int64_t vi = it / n_col;
+    const int j = static_cast<int>(it - vi * n_col) * 32 + lane;   // this lane's float4 column
+    const int64_t gi = vi / kQB;
+    const int i = static_cast<int>(vi - gi * kQB);
     const int b = static_cast<int>(gi / per_seq);
     const int rem = static_cast<int>(gi - static_cast<int64_t>(b) * per_seq);
     const int h = rem / p.row_blocks;
@@ -288,7 +293,7 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
         a[k] = (j < d4 && s0 + k < S) ? acc[static_cast<int64_t>(s0 + k) * d4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
     };
     float4 a[32];
-    load_batch(lane, 0, a);   // in flight together with the m / l loads
+    load_batch(j, 0, a);   // in flight together with the m / l loads
     float mv[2], lv[2];
     bool live[2];
 #pragma unroll
@@ -313,28 +318,26 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     const bool dead = M == -INFINITY;
     const float sc = p.v_scale / L;
-    for (int j0 = 0; j0 < d4; j0 += 32) {   // every lane runs every pass: the shuffles need the whole warp
-      const int j = j0 + lane;
-      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s0 = 0; s0 < S; s0 += 32) {
-        if (j0 > 0 || s0 > 0) load_batch(j, s0, a);
-        const float wsrc = s0 == 0 ? wv[0] : wv[1];
+    // every lane runs every step (the shuffles need the whole warp); lanes past the row store nothing
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      if (s0 > 0) load_batch(j, s0, a);
+      const float wsrc = s0 == 0 ? wv[0] : wv[1];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (s0 + k >= S) break;
-          const float w = __shfl_sync(0xffffffffu, wsrc, k);
-          if (w != -1.f) {
-            A.x += w * a[k].x;
-            A.y += w * a[k].y;
-            A.z += w * a[k].z;
-            A.w += w * a[k].w;
-          }
+      for (int k = 0; k < 32; ++k) {
+        if (s0 + k >= S) break;
+        const float w = __shfl_sync(0xffffffffu, wsrc, k);
+        if (w != -1.f) {
+          A.x += w * a[k].x;
+          A.y += w * a[k].y;
+          A.z += w * a[k].z;
+          A.w += w * a[k].w;
         }
       }
-      if (j < d4)
-        reinterpret_cast<float4*>(p.out + orow * p.d)[j] =
-            dead ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A.x * sc, A.y * sc, A.z * sc, A.w * sc);
     }
+    if (j < d4)
+      reinterpret_cast<float4*>(p.out + orow * p.d)[j] =
+          dead ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A.x * sc, A.y * sc, A.z * sc, A.w * sc);
   }
 }
 
@@ -350,8 +353,8 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
   else e = decode_dispatch_E4M3(p, q_dtype, grid_limit, stream);
   if (e != cudaSuccess) return e;
   if (p.max_splits <= 1) return cudaSuccess;   // every sequence has one split: the partials are the output
-  const int64_t items = static_cast<int64_t>(p.batch) * p.h_kv * p.row_blocks * kQB;
-  int64_t grid = static_cast<int64_t>(device_info().sm_count) * 16;
+  const int64_t items = static_cast<int64_t>(p.batch) * p.h_kv * p.row_blocks * kQB * ((p.d / 4 + 31) / 32);
+  int64_t grid = static_cast<int64_t>(device_info().sm_count) * 24;
   if (grid > items) grid = items;
   return launch_pdl(decode_merge_kernel, static_cast<unsigned>(grid), kDecodeMergeThreads, 0, stream, p);
 }
