@@ -22,6 +22,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import statistics
@@ -89,11 +90,23 @@ def attention_flops(case) -> float:
     return 4.0 * cfg.d * cfg.h_q * n_vis
 
 
+_SOURCE_TOKEN = re.compile(r'"(?:\\.|[^"\\\n])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(text: str) -> str:
+    """The source without its comments, blank lines and runs of whitespace (string literals, such as
+    inline PTX, kept): what decides the compiled kernel."""
+    text = _SOURCE_TOKEN.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return "\n".join(line for line in (" ".join(raw.split()) for raw in text.splitlines()) if line)
+
+
 def kernel_source_hash() -> str:
+    """Identifies the kernel code the committed ncu counters were taken on; a change to comments
+    alone keeps it."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

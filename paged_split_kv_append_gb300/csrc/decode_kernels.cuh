@@ -14,12 +14,15 @@
 //    (TensorFold PR #1219, the rows-first grid). A unit covers kQB = 4 query vectors (rows x
 //    GQA heads of one KV head): each K/V tile is read once for the whole GQA group.
 //  * One producer warp streams 16-position page tiles of one KV head (one contiguous block of
-//    the pool each, two per stage) into a ring of shared-memory stages with cp.async.bulk,
-//    completing on mbarrier transaction counts, and stages every unit's query vectors and
-//    metadata. It runs ahead across unit boundaries. A tile never straddles a page: split
-//    starts are page aligned and 16 divides the page.
+//    the pool each, two per stage) into a ring of shared-memory stages: tiles of 4 KB or less
+//    with 16-byte cp.async copies by its 32 lanes (each lane's completion arrives on the stage's
+//    mbarrier), larger ones with one cp.async.bulk each (completing on the transaction count).
+//    It also stages every unit's query vectors and metadata and runs ahead across unit
+//    boundaries. A tile never straddles a page: split starts are page aligned and 16 divides the
+//    page.
 //  * Every consumer warp takes a fixed quarter of every stage (so every partial sum has a
-//    fixed order, and the stages are consumed in ring order by all warps). Scores: LPT lanes share one position and each
+//    fixed order, and the stages are consumed in ring order by all warps). Scores: LPT lanes
+//    share one position and each
 //    holds 16 elements of the 4 query vectors as packed fp32 pairs (fma.rn.f32x2); a lane group
 //    scores TPG positions per pass and a transposing shuffle reduction leaves each lane with one
 //    (position, vector) score. Online softmax in log2 units with a lazy rescale: the running max
@@ -30,8 +33,9 @@
 //    unit's last stage, held back from the producer until the merge has read it (this frees the
 //    room of a fourth stage), or a double-buffered scratch for E4M3 stages, which are too small;
 //    bounded barriers order the writes and reads. A one-split sequence writes its normalised
-//    output; otherwise the unit stores its partial and decode_merge_kernel (launched after it)
-//    merges the splits in ascending order. No atomics on values and fixed reduction orders:
+//    output; otherwise the unit stores its partial, with an L2 evict-last policy so that it is
+//    still in L2 when decode_merge_kernel (launched after it) merges the splits in ascending
+//    order. No atomics on values and fixed reduction orders:
 //    the output is bit-identical under any schedule and any physical page placement.
 //  * Every wait is bounded; on timeout the kernel records NBX_DEV_TIMEOUT, lets its copies in
 //    flight land and returns.
