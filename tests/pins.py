@@ -69,7 +69,7 @@ def brute_force(case: wl.Case) -> np.ndarray:
         mask = torch.arange(L)[None, :] <= pos[:, None]         # [R, L]
         o = F.scaled_dot_product_attention(Q[None], K[None], V[None], attn_mask=mask[None, None],
                                            scale=case.scale)[0]  # [Hq, R, D]
-        o = torch.nan_to_num(o, nan=0.0)                        # rows with no visible key
+        o[:, ~mask.any(dim=1)] = 0.0                            # rows with no visible key (a NaN input stays NaN)
         out[b] = o.permute(1, 0, 2).numpy()
     return out
 
@@ -97,6 +97,52 @@ def pin_merge_partitions(case: wl.Case, seed: int = 0) -> float:
     rule, _ = op.decode_attention_split(case.q.float().numpy(), kp, vp, cfg.pool_dtype, case.block_table,
                                         case.lens, cfg.page_tokens, case.scale, case.k_scale, case.v_scale)
     return float(max(np.max(np.abs(split - one)), np.max(np.abs(rule - one))))
+
+
+def nan_aware_error(got: np.ndarray, want: np.ndarray) -> float:
+    """Max |got - want| over the outputs that are finite in both; inf when the two are not NaN at
+    exactly the same outputs."""
+    gn, wn = np.isnan(got), np.isnan(want)
+    if not np.array_equal(gn, wn):
+        return float("inf")
+    ok = ~gn
+    return float(np.max(np.abs(got[ok] - want[ok]))) if np.any(ok) else 0.0
+
+
+def pin_split_vs_brute_force(case: wl.Case, seed: int = 0) -> float:
+    """The split path (per-split partials, then the fixed-order merge) against brute force, under the
+    split rule and under random partitions (empty splits included): NaN at exactly the outputs where
+    torch's float64 attention gives NaN, 0 where a row sees no key, the rest equal to ~1e-12. This pins
+    the merge's skip rule on non-finite and empty inputs, which finite partitions never reach."""
+    kp, vp = oracle_pools(case)
+    cfg = case.cfg
+    rng = np.random.default_rng(seed)
+    want = brute_force(case)
+
+    def bounds(b, L):
+        n = int(rng.integers(1, 9))
+        cuts = np.sort(rng.integers(0, L + 1, size=n - 1)) if n > 1 else np.array([], dtype=np.int64)
+        return [0] + [int(c) for c in cuts] + [L]
+
+    err = 0.0
+    for fn in (None, bounds):
+        got, _ = op.decode_attention_split(case.q.float().numpy(), kp, vp, cfg.pool_dtype, case.block_table,
+                                           case.lens, cfg.page_tokens, case.scale, case.k_scale, case.v_scale,
+                                           bounds_fn=fn)
+        err = max(err, nan_aware_error(got, want))
+    return err
+
+
+def nan_case() -> wl.Case:
+    """A multi-row case whose outputs reach both unusual branches of the merge: a sequence shorter
+    than the window (its first rows see no key: every split is empty), a NaN key that every row of
+    its sequence sees, and a NaN in one element of one value."""
+    cfg = wl.CONFIGS["verify_small"]
+    cfg = type(cfg)(**{**cfg.__dict__, "rows": 4, "h_q": 6, "h_kv": 2, "d": 64, "page_tokens": 16})
+    case = wl.make_case(cfg, lens=[3, 50, 130, 600])
+    case.k_raw[int(case.tok_offset[1]) + 5, 0, 7] = float("nan")      # sequence 1, KV head 0, position 5
+    case.v_raw[int(case.tok_offset[3]) + 300, 1, 11] = float("nan")   # sequence 3, KV head 1, position 300
+    return case
 
 
 def pin_bf16_vs_torch(x: np.ndarray) -> int:

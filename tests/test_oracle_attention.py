@@ -168,3 +168,16 @@ def test_workload_inputs_are_seeded():
     assert torch.equal(a.k_raw, b.k_raw) and torch.equal(a.q, b.q)
     ids = a.block_table[a.block_table >= 0]
     assert len(np.unique(ids)) == ids.size and ids.max() < a.num_pages
+
+
+def test_split_path_matches_brute_force_with_nan_and_empty_rows():
+    case = pins.nan_case()
+    want = pins.brute_force(case)
+    G = case.cfg.group
+    # the brute force itself shows both branches: NaN outputs and rows with no key
+    assert np.all(np.isnan(want[1, :, :G])) and not np.any(np.isnan(want[1, :, G:]))
+    assert np.all(np.isnan(want[3, :, G:, 11])) and not np.any(np.isnan(np.delete(want[3, :, G:], 11, axis=-1)))
+    assert np.all(want[0, 0] == 0.0)
+    assert pins.pin_split_vs_brute_force(case) < 1e-12
+    # the one-pass oracle agrees with the brute force on the same outputs
+    assert pins.nan_aware_error(pins.oracle_output(case), want) < 1e-12

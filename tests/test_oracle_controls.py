@@ -136,3 +136,31 @@ def test_control_split_rule_without_page_alignment(monkeypatch):
     monkeypatch.setattr(op, "split_plan", unaligned)
     starts = [x for L in (300, 1000, 5000) for x in op.split_bounds(L, 16)[:-1] if x < L]
     assert any(x % 16 for x in starts)
+
+
+def test_control_merge_skips_unless_sum_positive(monkeypatch):
+    # the rule of TensorFold PR #1219 ("Gotchas"): a chunk takes part only when its sum of weights is
+    # positive. A split holding a NaN key has a NaN sum, so the rule drops it and hides the NaN.
+    orig = op.merge
+
+    def positive_sum_only(m, l, acc):
+        m = np.array(m, dtype=np.float64)
+        m[~(np.asarray(l, dtype=np.float64) > 0)] = -np.inf
+        return orig(m, l, acc)
+    case = pins.nan_case()
+    assert pins.pin_split_vs_brute_force(case) < TOL
+    monkeypatch.setattr(op, "merge", positive_sum_only)
+    assert pins.pin_split_vs_brute_force(case) > 1e-3
+
+
+def test_control_merge_of_no_live_split_is_nan(monkeypatch):
+    # a merge that takes M over every split: with no visible key M = -inf and exp(m - M) = NaN
+
+    def max_over_all(m, l, acc):
+        m = np.asarray(m, dtype=np.float64)
+        with np.errstate(invalid="ignore"):
+            w = np.exp(m - m.max())
+        return (w[:, None] * np.asarray(acc)).sum(axis=0) / (w * np.asarray(l)).sum()
+    case = pins.nan_case()
+    monkeypatch.setattr(op, "merge", max_over_all)
+    assert pins.pin_split_vs_brute_force(case) > 1e-3
