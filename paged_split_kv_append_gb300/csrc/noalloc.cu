@@ -12,9 +12,12 @@
 // the library holds it until the process exits. In host code the array's name only stands for
 // it; its device address is looked up with cudaGetSymbolAddress, once per device, on the first
 // call made with that device current. That first call should therefore come before any stream
-// capture. All calls share the one array and it keeps the contents of the last call: the kernels
-// rewrite everything they read (the plan kernel zeroes the work counter each call), and calls
-// that overlap on the GPU (two streams, or two threads) race on it.
+// capture. The address is kept for the life of the process: it does not survive a
+// cudaDeviceReset of that device (or a different context made current on it), after which this
+// entry point must not be called in the same process. All calls share the one array and it
+// keeps the contents of the last call: the kernels rewrite everything they read (the plan kernel
+// zeroes the work counter each call), and calls that overlap on the GPU (two streams, or two
+// threads) race on it.
 #include <cstdint>
 #include <mutex>
 

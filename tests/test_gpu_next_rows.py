@@ -2,8 +2,9 @@
 
 - The graph-replayable decode step (nbxtensor/ops/paged_decode_attn.py, paged_kv_append_step_kernel
   and paged_lens_advance_kernel): positions come from the device lengths, which then advance, so
-  one recorded step replays unchanged. Checked bit for bit against the separate append + decode
-  calls, which the parity tests check against the oracle.
+  one recorded step replays unchanged. Checked against the oracle (pools bit for bit, outputs within
+  the decode tolerance) after the first step and after a graph-replayed second step, and bit for bit
+  against the separate append + decode calls.
 - The contiguous (non-paged) decode (nbxtensor/ops/attention_wrappers.py, _decode_attn_vec): a
   [batch, h_kv, capacity, d] cache read as one page per sequence. Checked against the oracle.
 - Multi-row windows below the tensor-core threshold (rows x group < 64) on the SIMT kernel, with
@@ -15,10 +16,11 @@ import pytest
 import torch
 
 import bench
+import oracle.paged as op
 import paged_split_kv_append_gb300 as nbx
 import workloads as wl
 from tests import pins
-from tests.test_gpu_parity import DEV, TOL, check_against_oracle, run_step
+from tests.test_gpu_parity import DEV, TOL, check_against_oracle, oracle_codes, pool_codes, run_step
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +36,22 @@ def built():
 def _slots(block_table: torch.Tensor, P: int, b: int, pos: np.ndarray) -> np.ndarray:
     bt = block_table.cpu().numpy()
     return (bt[b, pos // P].astype(np.int64) * P + pos % P).astype(np.int32)
+
+
+def _check_step_against_oracle(case, kp, vp, lens, q, k_pool, v_pool, out):
+    """Pools bit for bit at every position the sequences hold, output within the tolerance of the
+    oracle's decode over those pools."""
+    cfg = case.cfg
+    P = cfg.page_tokens
+    pages = np.concatenate([case.block_table[b, np.arange(int(L)) // P] for b, L in enumerate(lens)])
+    pos = np.concatenate([np.arange(int(L)) % P for L in lens])
+    for gpu_pool, ora in ((k_pool, kp), (v_pool, vp)):
+        got = pool_codes(gpu_pool, cfg.pool_dtype)[pages, :, pos, :]
+        assert np.array_equal(got, oracle_codes(ora, cfg.pool_dtype)[pages, :, pos, :]), "step append not bit-exact"
+    want = op.decode_attention(q.float().cpu().numpy(), kp, vp, cfg.pool_dtype, case.block_table,
+                               np.asarray(lens), P, case.scale, case.k_scale, case.v_scale)
+    err = float(np.max(np.abs(out.cpu().numpy().astype(np.float64) - want)))
+    assert err <= TOL[cfg.pool_dtype], f"step: max abs error {err}"
 
 
 # ------------------------------------------------------------------------------------ decode step
@@ -67,6 +85,8 @@ def test_decode_step_matches_append_then_decode_and_replays(rows, h_q, h_kv, d, 
                                         case.scale, case.k_scale, case.v_scale)
     assert torch.equal(out, out_ref2)
     assert float((out - out_ref).abs().max()) <= TOL[pool]
+    kp, vp = pins.oracle_pools(case)                  # the oracle appends the same tokens at the same slots
+    _check_step_against_oracle(case, kp, vp, case.lens, ref.q, k_pool, v_pool, out)
 
     # a second step from a recorded graph: new keys at lens .. lens + rows - 1, lens advance again
     g = torch.Generator(device=DEV).manual_seed(7)
@@ -100,6 +120,11 @@ def test_decode_step_matches_append_then_decode_and_replays(rows, h_q, h_kv, d, 
     torch.cuda.synchronize()
     assert torch.equal(k_pool.view(torch.uint8), ref.k_pool.view(torch.uint8))
     assert torch.equal(out2, want)
+    # and the oracle: step 2's own new tokens appended at the slots after step 1's lengths
+    slots_np = slots.astype(np.int32)
+    op.append(kp, new_k2.view(B * rows, h_kv, d).cpu().numpy(), slots_np, P, pool, case.k_scale)
+    op.append(vp, new_v2.view(B * rows, h_kv, d).cpu().numpy(), slots_np, P, pool, case.v_scale)
+    _check_step_against_oracle(case, kp, vp, case.lens + rows, ref.q, k_pool, v_pool, out2)
 
 
 def test_decode_step_refuses_positions_past_the_bound():

@@ -15,11 +15,12 @@ import torch
 import bench
 import paged_split_kv_append_gb300 as nbx
 import workloads as wl
+from tests import pins
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-TOL = 2e-3           # bf16 pool, fp32 output: the tolerance of the decode parity tests
+TOL = {"bf16": 2e-3, "e4m3": 3e-2}   # fp32 output against the oracle: the decode parity tolerance
 SCRATCH = 32 * 1024 * 1024
 
 
@@ -44,18 +45,26 @@ def _call(f, sess, out, status):
              ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(status.data_ptr()), stream)
 
 
-@pytest.mark.parametrize("name", ["single_row", "ragged_small"])
-def test_noalloc_decode_matches_the_workspace_decode_twice(name):
+@pytest.mark.parametrize("name,kernel", [("single_row", nbx.PARTIAL_SIMT), ("ragged_small", nbx.PARTIAL_SIMT),
+                                         ("verify_small", nbx.PARTIAL_TCGEN05),
+                                         ("prefill_small", nbx.PARTIAL_TCGEN05_WIDENED)])
+def test_noalloc_decode_matches_the_workspace_decode_twice(name, kernel):
+    # the same kernels with the same plan as the workspace entry point: the outputs are equal bit for bit
     nbx.build()
     lib = nbx.lib()
     f = _noalloc(lib)
     case = wl.make_case(name, device=DEV)
+    cfg = case.cfg
     sess = bench.session_for_case(case, DEV)
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.dtype_code(sess.q), nbx.dtype_code(sess.k_pool), cfg.rows, cfg.h_q,
+                                               cfg.h_kv, cfg.d, 1, cfg.page_tokens) == kernel
     ref = sess.step().clone()                  # the existing entry point, with its own workspace
     torch.cuda.synchronize()
     assert sess.status_bits() == 0
-    need = nbx.nbx_paged_decode_workspace_bytes(case.cfg.batch, case.cfg.rows, case.cfg.h_q, case.cfg.h_kv,
-                                                case.cfg.d, case.max_seq_len)
+    # the fixed scratch holds what this call needs, including the bf16 copies of an fp8 window
+    need = nbx.nbx_paged_decode_workspace_bytes_for(nbx.dtype_code(case.q), nbx.dtype_code(sess.k_pool), cfg.batch,
+                                                    cfg.rows, cfg.h_q, cfg.h_kv, cfg.d, case.max_seq_len,
+                                                    cfg.page_tokens)
     assert need <= SCRATCH
     for _ in range(2):                         # two calls in a row share the library's scratch
         out = torch.full_like(ref, float("nan"))
@@ -63,8 +72,11 @@ def test_noalloc_decode_matches_the_workspace_decode_twice(name):
         assert _call(f, sess, out, status) == 0
         torch.cuda.synchronize()
         assert int(status.item()) == 0
-        err = float((out - ref).abs().max().item())
-        assert err <= TOL, err
+        assert torch.equal(out, ref)
+    if name != "single_row":                   # small enough for the oracle to compute every output
+        want = pins.oracle_output(case)
+        err = float(np.max(np.abs(out.cpu().numpy().astype(np.float64) - want)))
+        assert err <= TOL[cfg.pool_dtype], err
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
