@@ -16,7 +16,7 @@ from __future__ import annotations
 
 import os
 
-# The CPU oracle leg is single-threaded and says so (its BLAS calls are matrix-vector products).
+# Each process of the CPU oracle leg runs one BLAS thread (the leg runs one process per core).
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -183,63 +183,156 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------------------ CPU oracle leg
-class OracleLeg:
-    """The float64 CPU oracle run on this host as the CPU baseline. Set-up (not timed) builds
-    the oracle's own pools with every prefill position. A timed sample is a bounded part of the
-    step: (sequence, KV head) groups taken in order, each with the oracle's append of that
-    sequence's new positions and attention for all of the group's query rows and heads."""
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
-    def __init__(self, case: "wl.Case"):
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+class OracleGroups:
+    """The float64 oracle on a fixed list of (sequence, KV head) groups, in one process.
+
+    Set-up (not timed) builds the oracle's own pools with every prefill position of the groups'
+    heads. A timed sample runs the groups in turn: the oracle's append of the sequence's new
+    positions (this head) and attention for all of the group's query rows and heads."""
+
+    def __init__(self, spec: dict):
         import oracle.paged as op
         self.op = op
-        self.case = case
-        cfg = case.cfg
-        self.kp = op.new_pool(case.num_pages, cfg.h_kv, cfg.page_tokens, cfg.d, cfg.pool_dtype)
-        self.vp = op.new_pool(case.num_pages, cfg.h_kv, cfg.page_tokens, cfg.d, cfg.pool_dtype)
-        self.q = case.q.float().cpu().numpy()
-        self.k_new, self.v_new, self.s_new = [], [], []
-        for b in range(cfg.batch):
-            L, n_new = int(case.lens[b]), int(case.n_new[b])
-            lo, hi = int(case.tok_offset[b]), int(case.tok_offset[b + 1])
-            slots = wl.slots_for(case.block_table, cfg.page_tokens, b, np.arange(L, dtype=np.int64))
-            kk = case.k_raw[lo:hi].cpu().numpy()
-            vv = case.v_raw[lo:hi].cpu().numpy()
-            op.append(self.kp, kk[:L - n_new], slots[:L - n_new], cfg.page_tokens, cfg.pool_dtype, case.k_scale)
-            op.append(self.vp, vv[:L - n_new], slots[:L - n_new], cfg.page_tokens, cfg.pool_dtype, case.v_scale)
-            self.k_new.append(kk[L - n_new:].copy())
-            self.v_new.append(vv[L - n_new:].copy())
-            self.s_new.append(slots[L - n_new:].copy())
+        self.spec = spec
+        P, dt = spec["page_tokens"], spec["pool_dtype"]
+        shape = (spec["num_pages"], spec["h_kv"], P, spec["d"])
+        self.kp = op.new_pool(*shape, dt)     # untouched pages of other heads stay unallocated
+        self.vp = op.new_pool(*shape, dt)
+        self.elt = {"f32": 4, "bf16": 2, "e4m3": 1}[dt]
+        for g in spec["groups"]:
+            L, n_new, hk = g["len"], g["n_new"], g["hk"]
+            slots = (g["bt"][np.arange(L) // P].astype(np.int64) * P + np.arange(L) % P).astype(np.int32)
+            g["slots"] = slots
+            op.append(self.kp[:, hk:hk + 1], g["k"][:L - n_new, None], slots[:L - n_new], P, dt, spec["k_scale"])
+            op.append(self.vp[:, hk:hk + 1], g["v"][:L - n_new, None], slots[:L - n_new], P, dt, spec["v_scale"])
         self.cursor = 0
-        self.elt = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.pool_dtype]
 
     def sample(self, budget_s: float):
         """Run groups until about budget_s seconds passed; returns (K/V bytes, seconds, groups)."""
-        op, case, cfg = self.op, self.case, self.case.cfg
-        G = cfg.group
-        n_groups = cfg.batch * cfg.h_kv
-        done, groups = 0, 0
+        op, sp = self.op, self.spec
+        P, dt, G = sp["page_tokens"], sp["pool_dtype"], sp["h_q"] // sp["h_kv"]
+        done, n = 0, 0
         t0 = time.perf_counter()
-        while True:
-            b, hk = divmod(self.cursor, cfg.h_kv)
-            if hk == 0:
-                op.append(self.kp, self.k_new[b], self.s_new[b], cfg.page_tokens, cfg.pool_dtype, case.k_scale)
-                op.append(self.vp, self.v_new[b], self.s_new[b], cfg.page_tokens, cfg.pool_dtype, case.v_scale)
-            heads = [(0, r, h) for r in range(cfg.rows) for h in range(hk * G, (hk + 1) * G)]
-            op.decode_attention(self.q[b:b + 1], self.kp, self.vp, cfg.pool_dtype, case.block_table[b:b + 1],
-                                case.lens[b:b + 1], cfg.page_tokens, case.scale, case.k_scale, case.v_scale,
-                                heads=heads)
-            done += int(case.lens[b]) * cfg.d * self.elt * 2
-            groups += 1
-            self.cursor = (self.cursor + 1) % n_groups
+        while sp["groups"]:
+            g = sp["groups"][self.cursor]
+            L, n_new, hk = g["len"], g["n_new"], g["hk"]
+            op.append(self.kp[:, hk:hk + 1], g["k"][L - n_new:, None], g["slots"][L - n_new:], P, dt, sp["k_scale"])
+            op.append(self.vp[:, hk:hk + 1], g["v"][L - n_new:, None], g["slots"][L - n_new:], P, dt, sp["v_scale"])
+            heads = [(0, r, h) for r in range(sp["rows"]) for h in range(hk * G, (hk + 1) * G)]
+            op.decode_attention(g["q"][None], self.kp, self.vp, dt, g["bt"][None], np.array([L]), P, sp["scale"],
+                                sp["k_scale"], sp["v_scale"], heads=heads)
+            done += L * sp["d"] * self.elt * 2
+            n += 1
+            self.cursor = (self.cursor + 1) % len(sp["groups"])
             el = time.perf_counter() - t0
             if el >= budget_s:
-                return done, el, groups
+                return done, el, n
+        return 0, time.perf_counter() - t0, 0
+
+
+def _oracle_worker(spec, conn):
+    """One oracle process: build, report ready, then run one timed sample per request."""
+    leg = OracleGroups(spec)
+    conn.send("ready")
+    while True:
+        budget = conn.recv()
+        if budget is None:
+            break
+        conn.send(leg.sample(budget))
+    conn.close()
+
+
+class OracleLeg:
+    """The float64 CPU oracle as the CPU baseline, on every core of this host: the step's
+    (sequence, KV head) groups are dealt, longest first, to one spawned process per core (each
+    with one BLAS thread), and a timed sample runs all of them for the same wall-clock budget."""
+
+    def __init__(self, case: "wl.Case", workers: int = 0):
+        cfg = case.cfg
+        groups = [(b, hk) for b in range(cfg.batch) for hk in range(cfg.h_kv) if int(case.lens[b]) > 0]
+        groups.sort(key=lambda x: -int(case.lens[x[0]]))
+        self.case = case
+        self.workers = max(1, min(workers or host_cores(), len(groups) or 1))
+        q = case.q.float().cpu().numpy()
+        k_raw, v_raw = case.k_raw.cpu().numpy(), case.v_raw.cpu().numpy()
+        specs = []
+        for w in range(self.workers):
+            mine = []
+            for b, hk in groups[w::self.workers]:
+                lo, hi = int(case.tok_offset[b]), int(case.tok_offset[b + 1])
+                mine.append({"b": b, "hk": hk, "len": int(case.lens[b]), "n_new": int(case.n_new[b]),
+                             "bt": case.block_table[b].copy(), "k": np.ascontiguousarray(k_raw[lo:hi, hk]),
+                             "v": np.ascontiguousarray(v_raw[lo:hi, hk]), "q": q[b]})
+            specs.append({"rows": cfg.rows, "h_q": cfg.h_q, "h_kv": cfg.h_kv, "d": cfg.d,
+                          "page_tokens": cfg.page_tokens, "pool_dtype": cfg.pool_dtype, "num_pages": case.num_pages,
+                          "scale": case.scale, "k_scale": case.k_scale, "v_scale": case.v_scale, "groups": mine})
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")     # never fork a process that holds a CUDA context
+        self.conns, self.procs = [], []
+        for spec in specs:
+            parent, child = ctx.Pipe()
+            proc = ctx.Process(target=_oracle_worker, args=(spec, child), daemon=True)
+            proc.start()
+            child.close()
+            self.conns.append(parent)
+            self.procs.append(proc)
+        for c in self.conns:
+            if c.recv() != "ready":
+                raise RuntimeError("oracle worker failed to start")
+        self.n_groups = len(groups)
+
+    def sample(self, budget_s: float):
+        """All workers run for about budget_s seconds; returns (K/V bytes, wall seconds, groups)."""
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send(budget_s)
+        res = [c.recv() for c in self.conns]
+        wall = time.perf_counter() - t0
+        return sum(r[0] for r in res), wall, sum(r[2] for r in res)
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except (OSError, BrokenPipeError):
+                pass
+        for p in self.procs:
+            p.join(timeout=30)
 
     def describe(self, groups: int) -> str:
         cfg = self.case.cfg
-        return (f"{groups} (sequence, KV head) groups of the {cfg.name} step (of {cfg.batch * cfg.h_kv} per step; "
-                f"each: the oracle's append of the sequence's new positions and attention for its "
-                f"{cfg.rows * cfg.group} query rows x heads), float64 numpy, 1 thread")
+        return (f"{groups} (sequence, KV head) groups of the {cfg.name} step (of {self.n_groups} per step; each: "
+                f"the oracle's append of the sequence's new positions and attention for its "
+                f"{cfg.rows * cfg.group} query rows x heads), float64 numpy, {self.workers} processes "
+                f"of one thread, groups dealt longest first")
 
 
 # ------------------------------------------------------------------------------------------ GPU leg
@@ -257,101 +350,158 @@ def replica_seed(cfg, rank: int) -> int:
     return cfg.seed + 1000 * rank
 
 
-def run_gpu(args, rank: int, world: int):
-    import paged_split_kv_append_gb300 as nbx
-    dev = torch.device("cuda", torch.cuda.current_device())
-    cfg = wl.CONFIGS[args.config]
-    seed = replica_seed(cfg, rank)
-    case = wl.make_case(cfg, device=dev, seed=seed)
+def pack_inputs(sess, dev):
+    """Move the step's device inputs into one packed device buffer (sections 256-byte aligned) and
+    return it with a pinned host copy of the same layout, so the inputs of a step travel in one
+    host-to-device copy. The session's tensors become views of the packed buffer."""
+    names = ("q", "block_table", "seq_lens", "new_k", "new_v", "new_slots")
+    tensors = [(n, getattr(sess, n)) for n in names if getattr(sess, n) is not None]
+    offs, total = [], 0
+    for _, t in tensors:
+        offs.append(total)
+        total += -(-(t.numel() * t.element_size()) // 256) * 256
+    dev_buf = torch.empty(max(total, 256), dtype=torch.uint8, device=dev)
+    host_buf = torch.empty(max(total, 256), dtype=torch.uint8, pin_memory=True)
+    for (n, t), o in zip(tensors, offs):
+        nb = t.numel() * t.element_size()
+        view = dev_buf[o:o + nb].view(t.dtype).view(t.shape)
+        view.copy_(t)
+        host_buf[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+        setattr(sess, n, view)
+    return dev_buf, host_buf, total
+
+
+def time_case(case, dev, steps: int, warmup: int, flush, sink, stream, e2e_steps: int = 0):
+    """Time one workload's step (a CUDA-graph replay of append + decode) and its decode call alone
+    (plan + partial + merge, eager), each with the L2 flushed before every timed iteration; with
+    e2e_steps, also the step end to end through the public API with host buffers."""
     sess = session_for_case(case, dev)
     torch.cuda.synchronize()
-    kv_bytes = case.kv_bytes()
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.zeros(max(2 * l2, 1 << 20) // 4, dtype=torch.float32, device=dev)
-    sink = torch.zeros(1, dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-
-    # warm-up (also configures the kernels before capture)
     with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 1)):
+        for _ in range(max(warmup, 1)):      # also configures the kernels before capture
             sess.step(stream=stream)
     stream.synchronize()
     if sess.status_bits() != 0:
         raise RuntimeError(f"device status {sess.status_bits():#x} after warm-up")
-
-    # the step as a CUDA graph: append + plan + partial, replayed per timed step
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         sess.step(stream=stream)
-    # our kernels per call: append (when the step has new tokens), plan, partial, and the merge
-    # when some sequence can have more than one split
-    merge = 1 if case.max_seq_len > 256 else 0
-    widen = 1 if partial_kernel_name(cfg).startswith("widen") else 0
-    decode_launches = 2 + merge + widen
-    launches_per_step = decode_launches + (1 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 0)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush_l2(flush, sink)
+            ev[i][0].record(stream)
+            graph.replay()
+            ev[i][1].record(stream)
+        for i in range(steps):               # the decode call alone, same flush discipline
+            flush_l2(flush, sink)
+            kev[i][0].record(stream)
+            sess.decode(stream=stream)
+            kev[i][1].record(stream)
+    stream.synchronize()
+    if sess.status_bits() != 0:
+        raise RuntimeError(f"device status {sess.status_bits():#x} after the timed steps")
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = [a.elapsed_time(b) for a, b in kev]
+    # our kernels per call: append (when the step has new tokens), plan, partial, the merge when some
+    # sequence can have more than one split, and the widen kernel of an fp8 window on tensor cores
+    widen = 1 if partial_kernel_name(case.cfg).startswith("widen") else 0
+    decode_launches = 2 + (1 if case.max_seq_len > 256 else 0) + widen
+    step_launches = decode_launches + (1 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 0)
+    r = dict(step_ms=step_ms, ms_per_step=sum(step_ms) / len(step_ms), dec_ms=sum(dec_ms) / len(dec_ms),
+             launches=(step_launches + decode_launches) * steps, partial=partial_kernel_name(case.cfg))
+    if e2e_steps:
+        # end to end: one H2D copy of the step's packed inputs from pinned memory, the step through
+        # the public API, one D2H copy of the output, per step
+        dev_buf, host_buf, h2d = pack_inputs(sess, dev)
+        host_out = torch.empty(sess.out.shape, dtype=sess.out.dtype, pin_memory=True)
+        e2e_ms = []
+        with torch.cuda.stream(stream):
+            for _ in range(e2e_steps):
+                flush_l2(flush, sink)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                dev_buf.copy_(host_buf, non_blocking=True)
+                sess.step(stream=stream)
+                host_out.copy_(sess.out, non_blocking=True)
+                b.record(stream)
+                stream.synchronize()
+                e2e_ms.append(a.elapsed_time(b))
+        if sess.status_bits() != 0:
+            raise RuntimeError(f"device status {sess.status_bits():#x} after the end-to-end steps")
+        r.update(e2e_ms=sum(e2e_ms) / len(e2e_ms), h2d=h2d, d2h=host_out.numel() * host_out.element_size())
+    del graph, sess
+    return r
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+
+def roofline(case, dec_ms: float, peaks) -> dict:
+    """The roof that bounds the decode call: tensor throughput when the step's arithmetic intensity
+    (FLOPs per K/V byte) is above the ridge of the two measured peaks, else HBM bandwidth."""
+    peak, tflops_peak, peak_kind = peaks
+    kv = case.kv_bytes()
+    flops = attention_flops(case)
+    achieved_gbs = kv / (dec_ms * 1e-3) / 1e9
+    if kv and flops / kv > tflops_peak * 1e12 / (peak * 1e9):
+        tf = flops / (dec_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(tf, 2), "peak": tflops_peak, "unit": "TFLOP/s",
+                "frac": round(tf / tflops_peak, 4),
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, dense bf16 burst)",
+                "algorithmic_flops_per_launch": int(flops), "kv_gbs": round(achieved_gbs, 2)}
+    return {"bound": "hbm", "achieved": round(achieved_gbs, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved_gbs / peak, 4), "frac_of_nominal_8000": round(achieved_gbs / 8000.0, 4),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s", "kv_gbs": round(achieved_gbs, 2)}
+
+
+# the pages' own figure next to the one workload it matches (other hardware: context, not a target)
+CONTEXT = {"verify": "TensorFold PR #1219 (rows-first grid): 16 query rows over 32k keys, 7.62 -> 4.67 ms "
+                     "on GB10 (other hardware and model; context only)"}
+
+
+def run_gpu(args, rank: int, world: int):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = wl.CONFIGS[args.config]
+    case = wl.make_case(cfg, device=dev, seed=replica_seed(cfg, rank))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.zeros(max(2 * l2, 1 << 20) // 4, dtype=torch.float32, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
-        with torch.cuda.stream(stream):
-            for i in range(args.steps):
-                flush_l2(flush, sink)
-                ev[i][0].record(stream)
-                graph.replay()
-                ev[i][1].record(stream)
-            # the dominant kernel alone (plan + partial, no append), same flush discipline
-            for i in range(args.steps):
-                flush_l2(flush, sink)
-                kev[i][0].record(stream)
-                sess.decode(stream=stream)
-                kev[i][1].record(stream)
-        stream.synchronize()
+        r = time_case(case, dev, args.steps, args.warmup, flush, sink, stream,
+                      e2e_steps=max(3, min(args.steps, 50)))
     barrier(world)
     torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    dec_ms = [a.elapsed_time(b) for a, b in kev]
-    if sess.status_bits() != 0:
-        raise RuntimeError(f"device status {sess.status_bits():#x} after the timed steps")
-    ms_per_step = sum(step_ms) / len(step_ms)
-    dec_ms_mean = sum(dec_ms) / len(dec_ms)
-
-    # end to end through the public API with host buffers: H2D of the step's inputs from pinned
-    # memory, the step, D2H of the output, per step
-    host_in = {k: t.cpu().pin_memory() for k, t in (("q", sess.q), ("bt", sess.block_table),
-                                                       ("lens", sess.seq_lens), ("nk", sess.new_k),
-                                                       ("nv", sess.new_v), ("ns", sess.new_slots))
-               if t is not None}
-    host_out = torch.empty(sess.out.shape, dtype=sess.out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
-    dst = {"q": sess.q, "bt": sess.block_table, "lens": sess.seq_lens, "nk": sess.new_k, "nv": sess.new_v,
-           "ns": sess.new_slots}
-    e2e_steps = max(3, min(args.steps, 50))
-    e2e_ms = []
-    with torch.cuda.stream(stream):
-        for i in range(e2e_steps):
-            flush_l2(flush, sink)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for k, t in host_in.items():
-                dst[k].copy_(t, non_blocking=True)
-            sess.step(stream=stream)
-            host_out.copy_(sess.out, non_blocking=True)
-            b.record(stream)
-            stream.synchronize()
-            e2e_ms.append(a.elapsed_time(b))
-    e2e_ms_mean = sum(e2e_ms) / len(e2e_ms)
-
-    t_max = all_reduce_max(ms_per_step, world)
-    dec_max = all_reduce_max(dec_ms_mean, world)
-    e2e_max = all_reduce_max(e2e_ms_mean, world)
-    total_bytes = all_reduce_sum(float(kv_bytes), world)
-    return dict(case=case, kv_bytes=kv_bytes, total_bytes=total_bytes, ms_per_step=t_max, dec_ms=dec_max,
-                e2e_ms=e2e_max, h2d=h2d, d2h=d2h, clocks=clocks.summary(),
-                launches=(launches_per_step + decode_launches) * args.steps, step_ms=step_ms,
-                partial=partial_kernel_name(cfg))
+    kv_bytes = case.kv_bytes()
+    out = dict(case=case, kv_bytes=kv_bytes, total_bytes=all_reduce_sum(float(kv_bytes), world),
+               ms_per_step=all_reduce_max(r["ms_per_step"], world), dec_ms=all_reduce_max(r["dec_ms"], world),
+               e2e_ms=all_reduce_max(r["e2e_ms"], world), h2d=r["h2d"], d2h=r["d2h"], clocks=clocks.summary(),
+               launches=r["launches"], step_ms=r["step_ms"], partial=r["partial"])
+    # every other workload, timed the same way (one GPU only: they are not replicas)
+    per = {}
+    if world == 1 and args.per_config:
+        peaks = measured_peaks()
+        steps = max(10, min(args.steps, 200))
+        for name in wl.FULL_CONFIGS:
+            if name == args.config:
+                continue
+            c = wl.make_case(wl.CONFIGS[name], device=dev, seed=wl.CONFIGS[name].seed)
+            with ClockSampler(dev.index) as clk:
+                rr = time_case(c, dev, steps, args.warmup, flush, sink, stream)
+            roof = roofline(c, rr["dec_ms"], peaks)
+            per[name] = {"partial_kernel": rr["partial"], "steps": steps, "us_per_step": round(rr["ms_per_step"] * 1e3, 3),
+                         "step_kv_gbs": round(c.kv_bytes() / (rr["ms_per_step"] * 1e-3) / 1e9, 2),
+                         "decode_us": round(rr["dec_ms"] * 1e3, 3), "kv_bytes": int(c.kv_bytes()),
+                         "roofline": {**roof, "traffic": profiled_traffic(name, c.kv_bytes())},
+                         "clocks": clk.summary()}
+            if name in CONTEXT:
+                per[name]["context"] = CONTEXT[name]
+            del c
+            torch.cuda.empty_cache()
+    out["per_config"] = per
+    return out
 
 
 def partial_kernel_name(cfg) -> str:
@@ -417,6 +567,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
     ap.add_argument("--impl", default="nbx", choices=["nbx", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work in the CPU leg")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="time only --config, not the other workloads")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -445,31 +597,19 @@ def main():
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    peak, tflops_peak, peak_kind = measured_peaks()
+    peaks = measured_peaks()
     ms = r["ms_per_step"]
     value = r["total_bytes"] / (ms * 1e-3) / 1e9
-    dec_achieved = r["kv_bytes"] / (r["dec_ms"] * 1e-3) / 1e9
-    flops = attention_flops(case)
-    # the roof that bounds the decode call: tensor throughput when the step's arithmetic intensity
-    # (FLOPs per K/V byte) is above the ridge of the two measured peaks, else HBM bandwidth
-    tensor_bound = flops / r["kv_bytes"] > tflops_peak * 1e12 / (peak * 1e9)
-    if tensor_bound:
-        roof = {"bound": "tensor", "achieved": round(flops / (r["dec_ms"] * 1e-3) / 1e12, 2), "peak": tflops_peak,
-                "unit": "TFLOP/s", "frac": round(flops / (r["dec_ms"] * 1e-3) / 1e12 / tflops_peak, 4),
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, dense bf16 burst)",
-                "algorithmic_flops_per_launch": int(flops)}
-    else:
-        roof = {"bound": "hbm", "achieved": round(dec_achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(dec_achieved / peak, 4), "frac_of_nominal_8000": round(dec_achieved / 8000.0, 4),
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                else "fallback 6.8 TB/s"}
+    roof = roofline(case, r["dec_ms"], peaks)
     traffic = profiled_traffic(case.cfg.name, r["kv_bytes"])
+    cpu_bytes, cpu_s, cpu_desc, cores = 0, 0.0, "skipped", 0
     if args.cpu_budget > 0:
         leg = OracleLeg(wl.make_case(case.cfg, device="cpu"))
-        cpu_bytes, cpu_s, n_groups = leg.sample(args.cpu_budget)
-        cpu_desc = leg.describe(n_groups)
-    else:
-        cpu_bytes, cpu_s, cpu_desc = 0, 0.0, "skipped"
+        try:
+            cpu_bytes, cpu_s, n_groups = leg.sample(args.cpu_budget)
+            cpu_desc, cores = leg.describe(n_groups), leg.workers
+        finally:
+            leg.close()
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -487,11 +627,11 @@ def main():
         "config": config_block(case, args),
         "roofline": {"kernel": f"decode call (plan_kernel + {r['partial']} + decode_merge_kernel)", **roof,
                      "us_per_launch": round(r["dec_ms"] * 1e3, 3), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": int(r["kv_bytes"]),
-                     "kv_gbs": round(dec_achieved, 2)},
+                     "algorithmic_bytes_per_launch": int(r["kv_bytes"])},
+        "per_config": r["per_config"],
         "cpu_baseline": {"value": round(cpu_bytes / cpu_s / 1e9, 4) if cpu_s > 0 else None, "unit": "GB/s",
-                         "cores": 1, "kind": "oracle", "sample": cpu_desc,
-                         "seconds": round(cpu_s, 3)},
+                         "cores": cores, "cpu_model": cpu_model(), "host_cores": host_cores(), "kind": "oracle",
+                         "sample": cpu_desc, "seconds": round(cpu_s, 3)},
         "e2e": {"value": round(r["total_bytes"] / (r["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(r["e2e_ms"], 6), "h2d_bytes_per_step": int(r["h2d"]),
                 "d2h_bytes_per_step": int(r["d2h"])},
@@ -505,19 +645,22 @@ def main():
 
 
 def run_reference(args):
-    """The reference arm: the float64 CPU oracle, as it stands, on this host's cores; every step a
-    bounded sample of the workload's step, sized so the whole run takes about two minutes."""
+    """The reference arm: the float64 CPU oracle, as it stands, on every core of this host; every step
+    a bounded sample of the workload's step, sized so the whole run takes about two minutes."""
     cfg = wl.CONFIGS[args.config]
     leg = OracleLeg(wl.make_case(cfg, device="cpu"))
-    per_step = min(2.0, max(0.02, 120.0 / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        leg.sample(per_step)
-    tot_bytes, tot_s, tot_groups = 0, 0.0, 0
-    for _ in range(args.steps):
-        b, s, g = leg.sample(per_step)
-        tot_bytes += b
-        tot_s += s
-        tot_groups += g
+    try:
+        per_step = min(2.0, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
+        for _ in range(args.warmup):
+            leg.sample(per_step)
+        tot_bytes, tot_s, tot_groups = 0, 0.0, 0
+        for _ in range(args.steps):
+            b, s, g = leg.sample(per_step)
+            tot_bytes += b
+            tot_s += s
+            tot_groups += g
+    finally:
+        leg.close()
     value = tot_bytes / tot_s / 1e9 if tot_s > 0 else None
     v = round(value, 4) if value else None
     line = {
@@ -526,7 +669,8 @@ def run_reference(args):
         "ms_per_step": round(tot_s / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded: workloads/)",
         "config": config_block(leg.case, args, arm="oracle"),
-        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": leg.workers, "cpu_model": cpu_model(),
+                         "host_cores": host_cores(), "kind": "oracle",
                          "sample": f"per step ~{per_step:.3f} s: " + leg.describe(tot_groups // max(1, args.steps))},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
