@@ -23,7 +23,8 @@ from . import _build
 __all__ = [
     "NBX_F32", "NBX_BF16", "NBX_E4M3", "NbxError", "NbxLibraryMissing", "build", "lib", "library_path",
     "nbx_paged_kv_append", "nbx_paged_decode_workspace_bytes", "nbx_paged_decode_attn",
-    "nbx_paged_decode_merge", "nbx_set_decode_grid_limit", "nbx_status_string", "dtype_code",
+    "nbx_paged_decode_merge", "nbx_set_decode_grid_limit", "nbx_set_decode_wait_test", "nbx_status_string",
+    "dtype_code",
     "DEV_BAD_SLOT", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
 ]
 
@@ -77,6 +78,8 @@ def _declare(l):
     l.nbx_paged_decode_partial_kernel.restype = i32
     l.nbx_set_decode_grid_limit.argtypes = [i32]
     l.nbx_set_decode_grid_limit.restype = None
+    l.nbx_set_decode_wait_test.argtypes = [ctypes.c_ulonglong, ctypes.c_ulonglong]
+    l.nbx_set_decode_wait_test.restype = None
     l.nbx_status_string.argtypes = [i32]
     l.nbx_status_string.restype = ctypes.c_char_p
     l.nbx_abi_version.argtypes = []
@@ -299,3 +302,9 @@ def nbx_paged_decode_partial_kernel(q_dtype: int, pool_dtype: int, rows: int, h_
 
 def nbx_set_decode_grid_limit(max_ctas: int) -> None:
     lib().nbx_set_decode_grid_limit(int(max_ctas))
+
+
+def nbx_set_decode_wait_test(wait_limit_ns: int = 0, producer_delay_ns: int = 0) -> None:
+    """Tests of the timeout path only: the SIMT partial kernel's wait bound (0 = the default 2 s) and
+    a delay before its producer warps start (0 = none)."""
+    lib().nbx_set_decode_wait_test(int(wait_limit_ns), int(producer_delay_ns))

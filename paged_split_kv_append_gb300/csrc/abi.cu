@@ -19,6 +19,10 @@ DeviceInfo g_info[kMaxDevices];
 bool g_info_ok[kMaxDevices];
 std::mutex g_info_mu;
 std::atomic<int> g_grid_limit{0};
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;   // 2 s: no wait of a correct run comes near it
+constexpr unsigned long long kMaxProducerDelayNs = 50000000ull;     // 50 ms
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<unsigned long long> g_producer_delay_ns{0};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool finite(float x) { return std::isfinite(x); }
@@ -67,6 +71,11 @@ NBX_API const char* nbx_status_string(int status) {
 }
 
 NBX_API void nbx_set_decode_grid_limit(int max_ctas) { g_grid_limit.store(max_ctas < 0 ? 0 : max_ctas); }
+
+NBX_API void nbx_set_decode_wait_test(unsigned long long wait_limit_ns, unsigned long long producer_delay_ns) {
+  g_wait_limit_ns.store(wait_limit_ns == 0 ? kDefaultWaitLimitNs : wait_limit_ns);
+  g_producer_delay_ns.store(producer_delay_ns > kMaxProducerDelayNs ? kMaxProducerDelayNs : producer_delay_ns);
+}
 
 NBX_API int nbx_paged_kv_append(const void* new_k, const void* new_v, int new_dtype, int n_tok, int h_kv, int d,
                                 void* k_pool, void* v_pool, int pool_dtype, int num_pages, int page_tokens,
@@ -208,6 +217,8 @@ static int decode_call(const void* q, int q_dtype, int batch, int rows, int h_q,
   p.widen_v = widen ? ws + w.widen_v : nullptr;
   p.widen_bt = widen ? reinterpret_cast<int32_t*>(ws + w.widen_bt) : nullptr;
   p.t64 = w.t64;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.producer_delay_ns = g_producer_delay_ns.load();
   {
     const double part_bytes = static_cast<double>(batch) * rows * h_q * w.max_splits * d * 4.0;
     p.keep_frac = static_cast<float>(part_bytes <= 67108864.0 ? 1.0 : 67108864.0 / part_bytes);

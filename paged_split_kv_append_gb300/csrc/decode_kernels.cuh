@@ -140,14 +140,16 @@ struct Carver {
   }
 };
 
-// Bounded wait that also gives up as soon as another warp of the CTA has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Bounded wait (limit_ns of wall time) that also gives up as soon as another warp of the CTA has
+// aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((i & 3u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 3u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -202,6 +204,25 @@ __device__ __forceinline__ void pv_step(uint32_t pb, uint32_t va, f32x2 (&acc2)[
   }
 }
 
+// The same, updating only the vectors whose bit is set in `mask` (the others do not see the
+// position): a masked vector's accumulator is left as it is, not multiplied by a zero weight, so a
+// NaN in a value row past its causal limit cannot reach it.
+template <class PT, int VPL>
+__device__ __forceinline__ void pv_step_masked(uint32_t pb, uint32_t va, f32x2 (&acc2)[kQB][VPL / 2], int mask) {
+  f32x2 p0, p1, p2, p3;
+  lds2x64(pb, p0, p1);
+  lds2x64(pb + 16, p2, p3);
+  f32x2 vf[VPL / 2];
+  lds_row_x2<PT, VPL>(va, vf);
+#pragma unroll
+  for (int k = 0; k < VPL / 2; ++k) {
+    if (mask & 1) acc2[0][k] = fma2(p0, vf[k], acc2[0][k]);
+    if (mask & 2) acc2[1][k] = fma2(p1, vf[k], acc2[1][k]);
+    if (mask & 4) acc2[2][k] = fma2(p2, vf[k], acc2[2][k]);
+    if (mask & 8) acc2[3][k] = fma2(p3, vf[k], acc2[3][k]);
+  }
+}
+
 // ------------------------------------------------------------------------------------ partial
 template <class PT, class QT, int D>
 __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBlocks)
@@ -249,6 +270,10 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
 
   if (warp == NW) {
     // ================================================================ producer warp
+    if (p.producer_delay_ns) {   // a test holds the producer back so that the consumers' waits run out
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < p.producer_delay_ns) __nanosleep(10000);
+    }
     uint32_t tile_seq = 0, unit_seq = 0;
     int u = 0;
     if (lane == 0) u = atomicAdd(&p.header[1], 1);
@@ -256,7 +281,8 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
     bool ok = true;
     while (ok) {
       const uint32_t slot = unit_seq & 1u;
-      if (lane == 0 && unit_seq >= 2) ok = wait_or_abort(&sm.qempty[slot], ((unit_seq >> 1) - 1) & 1u, abort_flag);
+      if (lane == 0 && unit_seq >= 2)
+        ok = wait_or_abort(&sm.qempty[slot], ((unit_seq >> 1) - 1) & 1u, abort_flag, p.wait_limit_ns);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       if (u >= n_units) {
@@ -323,7 +349,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
         int okbits = 0;
         if (lane == 0) {
           if (tile_seq >= static_cast<uint32_t>(NS))
-            ok = wait_or_abort(&sm.empty[stage], ((tile_seq / NS) - 1) & 1u, abort_flag);
+            ok = wait_or_abort(&sm.empty[stage], ((tile_seq / NS) - 1) & 1u, abort_flag, p.wait_limit_ns);
           if (ok) {
             uint32_t bytes = 0;
 #pragma unroll
@@ -414,7 +440,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
   // bounded barrier over the consumer threads (an mbarrier: a warp that gave up cannot hang the others)
   auto csync = [&]() -> bool {
     mbar_arrive(sm.cbar);
-    const bool r = wait_or_abort(sm.cbar, cphase & 1u, abort_flag);
+    const bool r = wait_or_abort(sm.cbar, cphase & 1u, abort_flag, p.wait_limit_ns);
     ++cphase;
     return r;
   };
@@ -427,7 +453,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
 
   for (;;) {
     const uint32_t slot = unit_seq & 1u;
-    if (!wait_or_abort(&sm.qfull[slot], (unit_seq >> 1) & 1u, abort_flag)) {
+    if (!wait_or_abort(&sm.qfull[slot], (unit_seq >> 1) & 1u, abort_flag, p.wait_limit_ns)) {
       ok = false;
       break;
     }
@@ -469,14 +495,16 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
     uint32_t last_stage = 0;   // the unit's last stage: held for the epilogue's scratch
     for (int t = 0; t < n_stages; ++t, ++tile_seq) {
       const uint32_t stage = tile_seq % NS;
-      if (!wait_or_abort(&sm.full[stage], (tile_seq / NS) & 1u, abort_flag)) {
+      if (!wait_or_abort(&sm.full[stage], (tile_seq / NS) & 1u, abort_flag, p.wait_limit_ns)) {
         ok = false;
         break;
       }
       const int okbits = sm.stage_ok[stage];
       if (okbits) {
         const int n0 = u_start + t * C::kStageTok;
-        const bool full_stage = (okbits == 3) && (n0 + C::kStageTok <= u_end);
+        // every position of the stage copied, inside the split, and seen by every vector of the unit
+        // (vector 0 has the unit's smallest causal limit)
+        const bool full_stage = (okbits == 3) && (n0 + C::kStageTok <= u_end) && (n0 + C::kStageTok - 1 <= mtp->pos[0]);
         const uint32_t st_base = stages_base + stage * C::kStageBytes;
 #pragma unroll 1
         for (int pass = 0; pass < C::kWarpPasses; ++pass) {
@@ -564,10 +592,17 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
             for (int pt = 0; pt < C::kPassTok; ++pt)
               pv_step<PT, VPL>(pb_addr + pt * kQB * 8, st_base + v_lane_off + (pbase + pt) * D * PT::kBytes, acc2);
           } else {
+            // a position updates only the vectors whose causal limit it is within
 #pragma unroll
-            for (int pt = 0; pt < C::kPassTok; ++pt)
-              if (((okbits >> ((pbase + pt) / kTileN)) & 1) && n0 + pbase + pt < u_end)
-                pv_step<PT, VPL>(pb_addr + pt * kQB * 8, st_base + v_lane_off + (pbase + pt) * D * PT::kBytes, acc2);
+            for (int pt = 0; pt < C::kPassTok; ++pt) {
+              const int n = n0 + pbase + pt;
+              if (((okbits >> ((pbase + pt) / kTileN)) & 1) && n < u_end) {
+                const int mask = (n <= mtp->pos[0] ? 1 : 0) | (n <= mtp->pos[1] ? 2 : 0) | (n <= mtp->pos[2] ? 4 : 0) |
+                                 (n <= mtp->pos[3] ? 8 : 0);
+                pv_step_masked<PT, VPL>(pb_addr + pt * kQB * 8, st_base + v_lane_off + (pbase + pt) * D * PT::kBytes,
+                                        acc2, mask);
+              }
+            }
           }
           __syncwarp();
         }

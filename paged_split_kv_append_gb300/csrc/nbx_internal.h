@@ -118,6 +118,10 @@ struct DecodeParams {
   // fraction of the split partials' lines written with an L2 evict-last policy: about 64 MB of them
   // stay resident for the merge (1 when they all fit)
   float keep_frac;
+  // the SIMT partial kernel's wait bound, and a delay before its producer warp starts (0 in normal
+  // use); set only through nbx_set_decode_wait_test, to make a bounded wait run out on purpose
+  uint64_t wait_limit_ns;
+  uint64_t producer_delay_ns;
 };
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);

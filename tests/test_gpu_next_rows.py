@@ -187,3 +187,27 @@ def test_multi_row_window_below_the_tensor_core_threshold(rows, h_q, h_kv, d, P)
     for limit in (1, 7, 1000):
         _, o2 = run_step(case, grid_limit=limit)
         assert torch.equal(o2, out), f"grid limit {limit}"
+
+
+def test_nan_past_a_rows_causal_limit_stays_out_of_that_row():
+    # A NaN value at the window's last position (the last row's own new token) is seen only by the
+    # last row: the earlier rows of the window must match the oracle, which never reads past a row's
+    # causal limit. A NaN key elsewhere reaches exactly the rows that see it.
+    rows, h_q, h_kv, d, P = 4, 16, 4, 128, 16
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, rows, h_q, h_kv, d, 1, P) == \
+        nbx.PARTIAL_SIMT
+    cfg = wl.Config("mr_nan", 4, rows, h_q, h_kv, d, P, "bf16", "bf16", 44, ("fixed", (100, 37, 256, 300)))
+    case = wl.make_case(cfg, device=DEV)
+    off = case.tok_offset
+    case.v_raw[int(off[0]) + 99, 1, 5] = float("nan")        # sequence 0, last position: row 3 only
+    case.v_raw[int(off[2]) + 254, 3, 0] = float("nan")       # sequence 2, next to last: rows 2 and 3
+    case.k_raw[int(off[3]) + 298, 2, 7] = float("nan")       # sequence 3, a key rows 2 and 3 see
+    sess, out = run_step(case)
+    assert sess.status_bits() == 0
+    want = pins.oracle_output(case)
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isnan(want).any()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    err = float(np.max(np.abs(got[ok] - want[ok])))
+    assert err <= TOL["bf16"], err

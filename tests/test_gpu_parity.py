@@ -172,6 +172,7 @@ def test_nan_key_reaches_the_output():
     G = case.cfg.group
     assert np.all(np.isnan(o[0, 0, :G]))           # query heads of KV head 0
     assert np.all(np.isfinite(o[0, 0, G:])) and np.all(np.isfinite(o[1]))
+    assert pins.nan_aware_error(o.astype(np.float64), pins.oracle_output(case)) <= TOL["bf16"]
 
 
 def test_split_of_only_nan_keys_reaches_the_output():
@@ -184,6 +185,27 @@ def test_split_of_only_nan_keys_reaches_the_output():
     G = case.cfg.group
     assert np.all(np.isnan(o[0, 0, G:2 * G]))
     assert np.all(np.isfinite(o[0, 0, :G])) and np.all(np.isfinite(o[1]))
+    assert pins.nan_aware_error(o.astype(np.float64), pins.oracle_output(case)) <= TOL["bf16"]
+
+
+def test_a_wait_that_runs_out_sets_the_timeout_bit_and_returns():
+    # every consumer warp's first wait (for its unit's queries) is bounded at 20 us while the producer
+    # warps are held back 20 ms: the waits run out, the kernel records NBX_DEV_TIMEOUT, lets its copies
+    # in flight land and returns. The call completes and the next call is correct.
+    case = wl.make_case("single_row_small", device=DEV)
+    sess = bench.session_for_case(case, DEV)
+    torch.cuda.synchronize()
+    try:
+        nbx.nbx_set_decode_wait_test(20_000, 20_000_000)
+        sess.step()
+        torch.cuda.synchronize()
+    finally:
+        nbx.nbx_set_decode_wait_test(0, 0)
+    assert sess.status_bits() & nbx.DEV_TIMEOUT
+    sess.status.zero_()
+    out = sess.decode().clone()
+    torch.cuda.synchronize()
+    check_against_oracle(case, sess, out)
 
 
 def test_bad_page_id_sets_status_and_skips():
