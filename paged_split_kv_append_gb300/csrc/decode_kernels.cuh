@@ -567,10 +567,12 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
           if constexpr (TPG == 2) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
 #pragma unroll
           for (int off = LPT; off < 32; off <<= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          const bool need = !(mx <= m_run + kTau);
+          // a NaN running max stays NaN: a later pass whose positions are all masked (max -inf) must
+          // not replace it, or the warp's state would read as empty and the NaN would be dropped
+          const bool need = !(mx <= m_run + kTau) && m_run == m_run;
           if (__any_sync(0xffffffffu, need)) {
             const float m_new = need ? mx : m_run;
-            const float f = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
+            const float f = need ? fast_exp2(m_run - m_new) : 1.f;
             m_run = m_new;
             l_run *= f;
 #pragma unroll

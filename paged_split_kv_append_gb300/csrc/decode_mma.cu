@@ -634,9 +634,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           for (int i = 0; i < w; ++i) mxa[i] = max_nan(mxa[i], mxa[i + w]);
         const float c = p.qk_scale_log2;
         const float mx = mxa[0] * c;
-        const bool grow = !(mx <= m_run + kMmaTau);
+        // a NaN running max stays NaN (a later tile the row cannot see, max -inf, must not replace it)
+        const bool grow = !(mx <= m_run + kMmaTau) && m_run == m_run;
         const float m_new = grow ? mx : m_run;
-        const float f = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
+        const float f = grow ? fast_exp2(m_run - m_new) : 1.f;
         if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
           // O holds the PVs of tiles g-t .. g-1: wait for the last, then rescale it in TMEM
           if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {

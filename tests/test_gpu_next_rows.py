@@ -189,19 +189,22 @@ def test_multi_row_window_below_the_tensor_core_threshold(rows, h_q, h_kv, d, P)
         assert torch.equal(o2, out), f"grid limit {limit}"
 
 
-def test_nan_past_a_rows_causal_limit_stays_out_of_that_row():
+@pytest.mark.parametrize("d,pool", [(128, "bf16"), (64, "bf16"), (256, "bf16"), (128, "e4m3"), (128, "f32")])
+def test_nan_past_a_rows_causal_limit_stays_out_of_that_row(d, pool):
     # A NaN value at the window's last position (the last row's own new token) is seen only by the
     # last row: the earlier rows of the window must match the oracle, which never reads past a row's
-    # causal limit. A NaN key elsewhere reaches exactly the rows that see it.
-    rows, h_q, h_kv, d, P = 4, 16, 4, 128, 16
-    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, rows, h_q, h_kv, d, 1, P) == \
-        nbx.PARTIAL_SIMT
-    cfg = wl.Config("mr_nan", 4, rows, h_q, h_kv, d, P, "bf16", "bf16", 44, ("fixed", (100, 37, 256, 300)))
+    # causal limit. A NaN key reaches exactly the rows that see it, including rows whose later
+    # positions in the same split are masked (the NaN must survive those).
+    rows, h_q, h_kv, P = 4, 16, 4, 16
+    code = {"f32": nbx.NBX_F32, "bf16": nbx.NBX_BF16, "e4m3": nbx.NBX_E4M3}[pool]
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, code, rows, h_q, h_kv, d, 1, P) == nbx.PARTIAL_SIMT
+    cfg = wl.Config("mr_nan", 4, rows, h_q, h_kv, d, P, pool, "bf16", 44, ("fixed", (100, 37, 256, 300)))
     case = wl.make_case(cfg, device=DEV)
     off = case.tok_offset
     case.v_raw[int(off[0]) + 99, 1, 5] = float("nan")        # sequence 0, last position: row 3 only
     case.v_raw[int(off[2]) + 254, 3, 0] = float("nan")       # sequence 2, next to last: rows 2 and 3
     case.k_raw[int(off[3]) + 298, 2, 7] = float("nan")       # sequence 3, a key rows 2 and 3 see
+    case.k_raw[int(off[3]) + 170, 0, 3] = float("nan")       # sequence 3, early in its second split
     sess, out = run_step(case)
     assert sess.status_bits() == 0
     want = pins.oracle_output(case)
@@ -210,4 +213,4 @@ def test_nan_past_a_rows_causal_limit_stays_out_of_that_row():
     assert np.array_equal(np.isnan(got), np.isnan(want))
     ok = ~np.isnan(want)
     err = float(np.max(np.abs(got[ok] - want[ok])))
-    assert err <= TOL["bf16"], err
+    assert err <= TOL[pool], err

@@ -178,3 +178,23 @@ def test_fp8_widened_missing_page_and_nan_code():
                               cfg.page_tokens, case.scale, case.k_scale, case.v_scale)
     keep = np.isfinite(ref)
     assert np.max(np.abs(o[:1][keep] - ref[keep])) <= 2e-3
+
+
+def test_nan_key_reaches_rows_whose_later_tiles_are_masked():
+    # prefill window: 128 rows at 1372..1499 of a 1500-position sequence; the last split is
+    # [1280, 1500). A NaN key at 1300 is seen by every row, and the rows before 1408 then meet
+    # 64-position tiles they cannot see: the NaN must survive those tiles (the oracle gives NaN
+    # for every row of that KV head) and stay out of the other heads.
+    case = wl.make_case("prefill_small", device=DEV)
+    case.k_raw[1300, 1, 9] = float("nan")
+    sess = bench.session_for_case(case, DEV)
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, 128, 24, 4, 256, 1, 64) == \
+        nbx.PARTIAL_TCGEN05_WIDENED
+    out = sess.step().clone()
+    torch.cuda.synchronize()
+    assert sess.status_bits() == 0
+    want = pins.oracle_output(case)
+    got = out.cpu().numpy().astype(np.float64)
+    G = case.cfg.group
+    assert np.all(np.isnan(want[0, :, G:2 * G]))
+    assert pins.nan_aware_error(got, want) <= 3e-2
