@@ -333,12 +333,20 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
       const int last_page = (en.end - 1) / P;
       int pc = en.start / P;
       int my_page = (pc + lane <= last_page) ? bt_row[pc + lane] : -1;
+      // page index and position in the page of the next tile, advanced tile by tile (no division)
+      int t_pi = pc, t_po = en.start - pc * P;
       for (int n0 = en.start; n0 < en.end; n0 += C::kStageTok) {
-        int pages[2];
+        int pages[2], pofs[2];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           const int nh = n0 + hf * kTileN;
-          const int pi = nh / P;
+          const int pi = t_pi;
+          pofs[hf] = t_po;
+          t_po += kTileN;
+          if (t_po == P) {
+            t_po = 0;
+            ++t_pi;
+          }
           if (nh < en.end && pi >= pc + 32) {   // warp-uniform: next chunk of page ids
             pc = pi;
             my_page = (pc + lane <= last_page) ? bt_row[pc + lane] : -1;
@@ -372,9 +380,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
 #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {
                 if (!((okbits >> hf) & 1)) continue;
-                const int nh = n0 + hf * kTileN;
-                const int64_t off =
-                    ((static_cast<int64_t>(pages[hf]) * p.h_kv + h) * P + (nh - (nh / P) * P)) * D * PT::kBytes;
+                const int64_t off = ((static_cast<int64_t>(pages[hf]) * p.h_kv + h) * P + pofs[hf]) * D * PT::kBytes;
                 bulk_g2s(dst + hf * C::kTileBytes, static_cast<const char*>(p.k_pool) + off, C::kTileBytes,
                          &sm.full[stage]);
                 bulk_g2s(dst + C::kHalfBytes + hf * C::kTileBytes, static_cast<const char*>(p.v_pool) + off,
@@ -395,9 +401,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             if (!((okbits >> hf) & 1)) continue;
-            const int nh = n0 + hf * kTileN;
-            const int64_t off =
-                ((static_cast<int64_t>(pages[hf]) * p.h_kv + h) * P + (nh - (nh / P) * P)) * D * PT::kBytes;
+            const int64_t off = ((static_cast<int64_t>(pages[hf]) * p.h_kv + h) * P + pofs[hf]) * D * PT::kBytes;
             const char* ks = static_cast<const char*>(p.k_pool) + off;
             const char* vs = static_cast<const char*>(p.v_pool) + off;
 #pragma unroll

@@ -241,18 +241,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// try_wait with a suspend-time hint: a thread whose phase has not completed is suspended until it
-// completes (or the hint expires) instead of spinning, so waiting warps leave the issue slots free.
-constexpr uint32_t kSuspendHintNs = 1000000;
-
+// try_wait: a thread whose phase has not completed may be suspended until it completes or a
+// system-dependent time limit passes, so waiting warps leave the issue slots free. (An explicit
+// suspend-time hint of 1 ms measured about 1 % slower on the SIMT partial.)
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
