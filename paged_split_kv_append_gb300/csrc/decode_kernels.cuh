@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
       }
       const int e_idx = u / unit_span;
       const int rem = u - e_idx * unit_span;
-      const int h = rem / p.row_blocks;
+      const int h = p.row_blocks == 1 ? rem : rem / p.row_blocks;
       const int rb = rem - h * p.row_blocks;
       const Entry en = p.entries[e_idx];   // carries its sequence's length and split count
       int u_next = 0;
@@ -311,15 +311,18 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeCfg<PT, QT, D>::kMinBloc
         const int nvalid = min(kQB, RG - q0);
         mt.nvec = nvalid;
         mt.pad = 0;
+        int r = p.rows == 1 ? 0 : q0 / p.group;   // query row and head of vector q0 + i, stepped
+        int g = q0 - r * p.group;
 #pragma unroll
         for (int i = 0; i < kQB; ++i) {
-          const int qi = q0 + i;
-          const int r = qi / p.group;
-          const int g = qi - r * p.group;
           const bool vq = i < nvalid;
           mt.pos[i] = vq ? en.len - p.rows + r : -1;
           mt.orow[i] = vq ? (static_cast<int64_t>(en.b) * p.rows + r) * p.h_q + static_cast<int64_t>(h) * p.group + g
                           : 0;
+          if (++g == p.group) {
+            g = 0;
+            ++r;
+          }
         }
         sm.meta[slot] = mt;
         mbar_arrive_expect_tx(&sm.qfull[slot], static_cast<uint32_t>(nvalid * D * QT::kBytes));
