@@ -221,6 +221,54 @@ NBX_API int nbx_decode_attn_contiguous(const void* q, int q_dtype, int batch, in
 NBX_API int nbx_paged_decode_merge(const float* acc_part, const float* m_part, const float* l_part, int n_rows,
                                    int splits, int d, float* out, void* stream);
 
+/*
+ * nbx_paged_decode_bounds -- the score bounds the fixed-shift softmax gates on.
+ * (maxdiffusion PR #477, "fixed-m": the per-head metadata computed before the kernel, here per query
+ * vector and per (sequence, KV head).)
+ *
+ * q_norm [device] fp32 [batch, rows, h_q]: |q| of every query vector.
+ * kv_max [device] fp32 [batch, h_kv, 2]: {max_j |k_j| * k_scale, max_{j,d} |v_jd| * v_scale} over the
+ * positions 0 .. seq_lens[b] - 1 of the sequence, read through the block table. A NaN input gives a
+ * NaN bound (which no gate passes). One pass over the sequences' K and V. Other arguments, rules and
+ * status bits as for nbx_paged_decode_attn (no workspace).
+ */
+NBX_API int nbx_paged_decode_bounds(const void* q, int q_dtype, int batch, int rows, int h_q, int d, const void* k_pool,
+                                    const void* v_pool, int pool_dtype, int num_pages, int h_kv, int page_tokens,
+                                    const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                    int max_seq_len, float k_scale, float v_scale, float* q_norm, float* kv_max,
+                                    int32_t* status, void* stream);
+
+/*
+ * nbx_paged_decode_attn_fixed_shift -- nbx_paged_decode_attn with the fixed-shift softmax of
+ * maxdiffusion PR #477 ("fixed-m") on the tensor-core kernel, as an ablation of the online max.
+ *
+ * For a query row of a split of n keys, U = |q| * max|k| * scale * log2(e) bounds every score in
+ * log2 units (Cauchy-Schwarz). With C(n) = 127 - ceil(log2 n) - ceil(log2 256) and the gate
+ * floor((C(n) + 125) / 2): a row with U <= gate and max |v| <= 256 takes its weights as 2^(z - m),
+ * m = ceil(U) - C(n), fixed before the split is read (no running max, no rescale; no weight above 2^C
+ * or below 2^-125). A row that fails the gate, and every row of a window whose P enters the product
+ * in f16 (an fp8 pool widened on tensor cores: f16 cannot hold 2^C), keeps the online max. Calls that
+ * run the SIMT kernel are the same as nbx_paged_decode_attn. Results are within the decode's tolerance
+ * of nbx_paged_decode_attn's.
+ *
+ *   q_norm, kv_max  [device] the bounds, as nbx_paged_decode_bounds writes them
+ *   every other argument as for nbx_paged_decode_attn.
+ */
+NBX_API int nbx_paged_decode_attn_fixed_shift(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
+                                              const void* k_pool, const void* v_pool, int pool_dtype, int num_pages,
+                                              int h_kv, int page_tokens, const int32_t* block_table, int max_pages,
+                                              const int32_t* seq_lens, int max_seq_len, float scale, float k_scale,
+                                              float v_scale, float* out, void* workspace, size_t workspace_bytes,
+                                              const float* q_norm, const float* kv_max, int32_t* status,
+                                              void* stream);
+
+/*
+ * nbx_decode_fixed_shift_gate -- the fixed-shift constants for n_keys keys and a value bound
+ * (maxdiffusion PR #477, get_fixed_m_constants): C = 127 - ceil(log2 n_keys) - ceil(log2 v_max_bound)
+ * and gate = floor((C + 125) / 2). Host-only. NBX_ERR_VALUE for n_keys < 1 or v_max_bound < 1.
+ */
+NBX_API int nbx_decode_fixed_shift_gate(int n_keys, double v_max_bound, int* c_out, int* gate_out);
+
 /* Bytes of device scratch that libnbx keeps for nbx_paged_decode_attn_noalloc (32 MiB). */
 #define NBX_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

@@ -24,6 +24,7 @@ __all__ = [
     "NBX_F32", "NBX_BF16", "NBX_E4M3", "NbxError", "NbxLibraryMissing", "build", "lib", "library_path",
     "nbx_paged_kv_append", "nbx_paged_decode_workspace_bytes", "nbx_paged_decode_attn",
     "nbx_paged_decode_merge", "nbx_set_decode_grid_limit", "nbx_set_decode_wait_test", "nbx_status_string",
+    "nbx_paged_decode_bounds", "nbx_paged_decode_attn_fixed_shift", "nbx_decode_fixed_shift_gate",
     "dtype_code",
     "DEV_BAD_SLOT", "DEV_BAD_PAGE", "DEV_BAD_LEN", "DEV_TIMEOUT",
 ]
@@ -80,6 +81,14 @@ def _declare(l):
     l.nbx_set_decode_grid_limit.restype = None
     l.nbx_set_decode_wait_test.argtypes = [ctypes.c_ulonglong, ctypes.c_ulonglong]
     l.nbx_set_decode_wait_test.restype = None
+    l.nbx_paged_decode_bounds.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp, i32, vp, i32,
+                                          f32, f32, vp, vp, vp, vp]
+    l.nbx_paged_decode_bounds.restype = i32
+    l.nbx_paged_decode_attn_fixed_shift.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, i32, i32, vp, i32,
+                                                    vp, i32, f32, f32, f32, vp, vp, sz, vp, vp, vp, vp]
+    l.nbx_paged_decode_attn_fixed_shift.restype = i32
+    l.nbx_decode_fixed_shift_gate.argtypes = [i32, ctypes.c_double, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    l.nbx_decode_fixed_shift_gate.restype = i32
     l.nbx_status_string.argtypes = [i32]
     l.nbx_status_string.restype = ctypes.c_char_p
     l.nbx_abi_version.argtypes = []
@@ -308,3 +317,74 @@ def nbx_set_decode_wait_test(wait_limit_ns: int = 0, producer_delay_ns: int = 0)
     """Tests of the timeout path only: the SIMT partial kernel's wait bound (0 = the default 2 s) and
     a delay before its producer warps start (0 = none)."""
     lib().nbx_set_decode_wait_test(int(wait_limit_ns), int(producer_delay_ns))
+
+
+def _decode_shapes(q, k_pool, v_pool, block_table, seq_lens):
+    for n, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("block_table", block_table),
+                 ("seq_lens", seq_lens)):
+        _cuda_contig(n, t)
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise ValueError("block_table and seq_lens must be int32")
+    if k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype:
+        raise ValueError("k_pool and v_pool must match")
+    batch, rows, h_q, d = q.shape
+    num_pages, h_kv, page_tokens, d_p = k_pool.shape
+    if d_p != d or block_table.dim() != 2 or block_table.shape[0] != batch or seq_lens.numel() != batch:
+        raise ValueError(f"q {list(q.shape)}, pool {list(k_pool.shape)}, block_table {list(block_table.shape)}, "
+                         f"seq_lens {list(seq_lens.shape)} do not fit")
+    return batch, rows, h_q, d, num_pages, h_kv, page_tokens, block_table.shape[1]
+
+
+def nbx_paged_decode_bounds(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor, block_table: torch.Tensor,
+                            seq_lens: torch.Tensor, max_seq_len: int, k_scale: float = 1.0, v_scale: float = 1.0,
+                            status: Optional[torch.Tensor] = None, stream=None):
+    """The fixed-shift softmax's score bounds: (q_norm [batch, rows, h_q], kv_max [batch, h_kv, 2]) fp32."""
+    batch, rows, h_q, d, num_pages, h_kv, page_tokens, max_pages = _decode_shapes(q, k_pool, v_pool, block_table,
+                                                                                  seq_lens)
+    q_norm = torch.empty((batch, rows, h_q), dtype=torch.float32, device=q.device)
+    kv_max = torch.empty((batch, h_kv, 2), dtype=torch.float32, device=q.device)
+    st = lib().nbx_paged_decode_bounds(_ptr(q), dtype_code(q), batch, rows, h_q, d, _ptr(k_pool), _ptr(v_pool),
+                                       dtype_code(k_pool), num_pages, h_kv, page_tokens, _ptr(block_table), max_pages,
+                                       _ptr(seq_lens), int(max_seq_len), float(k_scale), float(v_scale), _ptr(q_norm),
+                                       _ptr(kv_max), _ptr(status), _stream(stream))
+    _check("nbx_paged_decode_bounds", st)
+    return q_norm, kv_max
+
+
+def nbx_paged_decode_attn_fixed_shift(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                                      block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                                      scale: float, q_norm: torch.Tensor, kv_max: torch.Tensor, k_scale: float = 1.0,
+                                      v_scale: float = 1.0, out: Optional[torch.Tensor] = None,
+                                      workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                                      stream=None) -> torch.Tensor:
+    """nbx_paged_decode_attn with the fixed-shift softmax where the bounds pass the gate."""
+    batch, rows, h_q, d, num_pages, h_kv, page_tokens, max_pages = _decode_shapes(q, k_pool, v_pool, block_table,
+                                                                                  seq_lens)
+    _cuda_contig("q_norm", q_norm)
+    _cuda_contig("kv_max", kv_max)
+    if q_norm.dtype != torch.float32 or kv_max.dtype != torch.float32 or q_norm.numel() != batch * rows * h_q or \
+            kv_max.numel() != batch * h_kv * 2:
+        raise ValueError("q_norm [batch, rows, h_q] and kv_max [batch, h_kv, 2] must be fp32")
+    if out is None:
+        out = torch.empty((batch, rows, h_q, d), dtype=torch.float32, device=q.device)
+    _cuda_contig("out", out)
+    need = nbx_paged_decode_workspace_bytes_for(dtype_code(q), dtype_code(k_pool), batch, rows, h_q, h_kv, d,
+                                                max_seq_len, page_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().nbx_paged_decode_attn_fixed_shift(_ptr(q), dtype_code(q), batch, rows, h_q, d, _ptr(k_pool),
+                                                 _ptr(v_pool), dtype_code(k_pool), num_pages, h_kv, page_tokens,
+                                                 _ptr(block_table), max_pages, _ptr(seq_lens), int(max_seq_len),
+                                                 float(scale), float(k_scale), float(v_scale), _ptr(out),
+                                                 _ptr(workspace), workspace.numel(), _ptr(q_norm), _ptr(kv_max),
+                                                 _ptr(status), _stream(stream))
+    _check("nbx_paged_decode_attn_fixed_shift", st)
+    return out
+
+
+def nbx_decode_fixed_shift_gate(n_keys: int, v_max_bound: float = 256.0):
+    """(C, gate) of the fixed-shift softmax for n_keys keys and a value bound (host-only)."""
+    c, g = ctypes.c_int(), ctypes.c_int()
+    st = lib().nbx_decode_fixed_shift_gate(int(n_keys), float(v_max_bound), ctypes.byref(c), ctypes.byref(g))
+    _check("nbx_decode_fixed_shift_gate", st)
+    return c.value, g.value

@@ -159,7 +159,8 @@ static int decode_call(const void* q, int q_dtype, int batch, int rows, int h_q,
                        const int32_t* block_table, int max_pages, const int32_t* seq_lens, int max_seq_len,
                        float scale, float k_scale, float v_scale, float* out, void* workspace,
                        size_t workspace_bytes, int32_t* status, cudaStream_t stream, bool identity,
-                       int32_t* lens_out, int len_add) {
+                       int32_t* lens_out, int len_add, const float* fs_q_norm = nullptr,
+                       const float* fs_kv_max = nullptr) {
   if (!decode_shape_ok(batch, rows, h_q, h_kv, d, max_seq_len)) return NBX_ERR_SHAPE;
   if (num_pages < 1 || page_tokens < 1 || max_pages < 1) return NBX_ERR_SHAPE;
   if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * page_tokens) return NBX_ERR_SHAPE;
@@ -218,6 +219,10 @@ static int decode_call(const void* q, int q_dtype, int batch, int rows, int h_q,
   p.widen_bt = widen ? reinterpret_cast<int32_t*>(ws + w.widen_bt) : nullptr;
   p.t64 = w.t64;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  p.fs_q_norm = fs_q_norm;
+  p.fs_kv_max = fs_kv_max;
+  p.fs_scale_log2 = scale * kLog2eHost;
+  p.k_scale_host = k_scale;
   p.producer_delay_ns = g_producer_delay_ns.load();
   {
     const double part_bytes = static_cast<double>(batch) * rows * h_q * w.max_splits * d * 4.0;
@@ -236,6 +241,65 @@ NBX_API int nbx_paged_decode_attn(const void* q, int q_dtype, int batch, int row
   return decode_call(q, q_dtype, batch, rows, h_q, d, k_pool, v_pool, pool_dtype, num_pages, h_kv, page_tokens,
                      block_table, max_pages, seq_lens, max_seq_len, scale, k_scale, v_scale, out, workspace,
                      workspace_bytes, status, static_cast<cudaStream_t>(stream), false, nullptr, 0);
+}
+
+NBX_API int nbx_paged_decode_attn_fixed_shift(const void* q, int q_dtype, int batch, int rows, int h_q, int d,
+                                              const void* k_pool, const void* v_pool, int pool_dtype, int num_pages,
+                                              int h_kv, int page_tokens, const int32_t* block_table, int max_pages,
+                                              const int32_t* seq_lens, int max_seq_len, float scale, float k_scale,
+                                              float v_scale, float* out, void* workspace, size_t workspace_bytes,
+                                              const float* q_norm, const float* kv_max, int32_t* status,
+                                              void* stream) {
+  if (batch > 0 && (q_norm == nullptr || kv_max == nullptr)) return NBX_ERR_NULL;
+  return decode_call(q, q_dtype, batch, rows, h_q, d, k_pool, v_pool, pool_dtype, num_pages, h_kv, page_tokens,
+                     block_table, max_pages, seq_lens, max_seq_len, scale, k_scale, v_scale, out, workspace,
+                     workspace_bytes, status, static_cast<cudaStream_t>(stream), false, nullptr, 0, q_norm, kv_max);
+}
+
+NBX_API int nbx_paged_decode_bounds(const void* q, int q_dtype, int batch, int rows, int h_q, int d, const void* k_pool,
+                                    const void* v_pool, int pool_dtype, int num_pages, int h_kv, int page_tokens,
+                                    const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                                    int max_seq_len, float k_scale, float v_scale, float* q_norm, float* kv_max,
+                                    int32_t* status, void* stream) {
+  if (!decode_shape_ok(batch, rows, h_q, h_kv, d, max_seq_len)) return NBX_ERR_SHAPE;
+  if (num_pages < 1 || page_tokens < 1 || max_pages < 1) return NBX_ERR_SHAPE;
+  if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_pages) * page_tokens) return NBX_ERR_SHAPE;
+  if (q_dtype != NBX_F32 && q_dtype != NBX_BF16) return NBX_ERR_DTYPE;
+  if (pool_dtype != NBX_F32 && pool_dtype != NBX_BF16 && pool_dtype != NBX_E4M3) return NBX_ERR_DTYPE;
+  if (!finite(k_scale) || !finite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f)) return NBX_ERR_VALUE;
+  if (batch == 0) return NBX_OK;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_lens || !q_norm || !kv_max) return NBX_ERR_NULL;
+  DecodeParams p = {};
+  p.q = q;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.status = status;
+  p.batch = batch;
+  p.rows = rows;
+  p.h_q = h_q;
+  p.h_kv = h_kv;
+  p.d = d;
+  p.num_pages = num_pages;
+  p.page_tokens = page_tokens;
+  p.max_pages = max_pages;
+  p.max_seq_len = max_seq_len;
+  p.v_scale = v_scale;
+  p.k_scale_host = k_scale;
+  const cudaError_t e = bounds_dispatch(p, q_dtype, pool_dtype, q_norm, kv_max, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NBX_OK : NBX_ERR_CUDA;
+}
+
+NBX_API int nbx_decode_fixed_shift_gate(int n_keys, double v_max_bound, int* c_out, int* gate_out) {
+  if (n_keys < 1 || !(v_max_bound >= 1.0) || !std::isfinite(v_max_bound) || !c_out || !gate_out) return NBX_ERR_VALUE;
+  int lg_n = 0;
+  while ((1ll << lg_n) < n_keys) ++lg_n;   // ceil(log2 n)
+  const int lg_v = static_cast<int>(std::ceil(std::log2(v_max_bound)));
+  *c_out = 127 - lg_n - lg_v;
+  const int w = *c_out + 125;
+  *gate_out = w >= 0 ? w / 2 : -((1 - w) / 2);   // floor(w / 2)
+  return NBX_OK;
 }
 
 NBX_API int nbx_decode_attn_contiguous(const void* q, int q_dtype, int batch, int rows, int h_q, int d,

@@ -341,6 +341,97 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
   }
 }
 
+// ------------------------------------------------------------------------------------ score bounds
+constexpr int kBoundsThreads = 256;
+
+// Score bounds for the fixed-shift softmax (maxdiffusion PR #477: the metadata computed before the
+// kernel, here per query vector and per (sequence, KV head)): |q| of every query vector, and
+// max_j |k_j| * k_scale and max_{j,d} |v_jd| * v_scale over the positions a sequence holds, read
+// through the block table. A NaN input gives a NaN bound, which no gate passes; a length out of
+// bounds is read as empty (NBX_DEV_BAD_LEN) and a page id outside the pool is skipped
+// (NBX_DEV_BAD_PAGE). One CTA per (sequence, KV head), a warp per position; the CTAs of KV head 0
+// also write the sequence's query norms.
+template <class PT, class QT>
+__global__ void __launch_bounds__(kBoundsThreads) bounds_kernel(DecodeParams p, float* q_norm, float* kv_max) {
+  __shared__ float s_k[kBoundsThreads / 32], s_v[kBoundsThreads / 32];
+  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.h_kv));
+  const int h = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * p.h_kv);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kBoundsThreads / 32;
+  int L = p.seq_lens[b];
+  if (L < 0 || L > p.max_seq_len || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * p.page_tokens) {
+    if (h == 0 && threadIdx.x == 0) raise_status(p.status, NBX_DEV_BAD_LEN);
+    L = 0;
+  }
+  float k2 = 0.f, va = 0.f;   // max |k|^2 and max |v| (pool units) over this warp's positions
+  for (int j = warp; j < L; j += kWarps) {
+    const int page = p.block_table[static_cast<int64_t>(b) * p.max_pages + j / p.page_tokens];
+    if (page < 0 || page >= p.num_pages) {
+      if (lane == 0) raise_status(p.status, NBX_DEV_BAD_PAGE);
+      continue;
+    }
+    const int64_t row = ((static_cast<int64_t>(page) * p.h_kv + h) * p.page_tokens + j % p.page_tokens) * p.d;
+    const char* kr = static_cast<const char*>(p.k_pool) + row * PT::kBytes;
+    const char* vr = static_cast<const char*>(p.v_pool) + row * PT::kBytes;
+    float ks = 0.f, vm = 0.f;
+    for (int e = 2 * lane; e < p.d; e += 64) {
+      const float2 kk = load_pair<PT>(kr + e * PT::kBytes);
+      const float2 vv = load_pair<PT>(vr + e * PT::kBytes);
+      ks = fmaf(kk.x, kk.x, fmaf(kk.y, kk.y, ks));
+      vm = max_nan(vm, max_nan(fabsf(vv.x), fabsf(vv.y)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ks += __shfl_xor_sync(0xffffffffu, ks, o);
+      vm = max_nan(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+    }
+    k2 = max_nan(k2, ks);
+    va = max_nan(va, vm);
+  }
+  if (lane == 0) {
+    s_k[warp] = k2;
+    s_v[warp] = va;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float kt = 0.f, vt = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      kt = max_nan(kt, s_k[w]);
+      vt = max_nan(vt, s_v[w]);
+    }
+    kv_max[2 * blockIdx.x] = sqrtf(kt) * p.k_scale_host;
+    kv_max[2 * blockIdx.x + 1] = vt * p.v_scale;
+  }
+  if (h != 0) return;
+  const int nq = p.rows * p.h_q;   // this sequence's query vectors
+  for (int v = warp; v < nq; v += kWarps) {
+    const char* qr = static_cast<const char*>(p.q) + (static_cast<int64_t>(b) * nq + v) * p.d * QT::kBytes;
+    float qs = 0.f;
+    for (int e = 2 * lane; e < p.d; e += 64) {
+      const float2 qq = load_pair<QT>(qr + e * QT::kBytes);
+      qs = fmaf(qq.x, qq.x, fmaf(qq.y, qq.y, qs));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
+    if (lane == 0) q_norm[static_cast<int64_t>(b) * nq + v] = sqrtf(qs);
+  }
+}
+
+cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, float* q_norm, float* kv_max,
+                            cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>(p.batch * p.h_kv);
+  if (q_dtype == NBX_F32) {
+    if (pool_dtype == NBX_F32) bounds_kernel<F32, F32><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+    else if (pool_dtype == NBX_BF16) bounds_kernel<BF16, F32><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+    else bounds_kernel<E4M3, F32><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+  } else {
+    if (pool_dtype == NBX_F32) bounds_kernel<F32, BF16><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+    else if (pool_dtype == NBX_BF16) bounds_kernel<BF16, BF16><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+    else bounds_kernel<E4M3, BF16><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit,
                             cudaStream_t stream) {
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);

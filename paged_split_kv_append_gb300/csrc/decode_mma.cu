@@ -598,7 +598,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int r = mu.mt * Rt + rt;
       const bool row_ok = rt < Rt && r < p.rows;
       const int pos = mu.len - p.rows + r;   // last position this row sees
-      float m_run = -INFINITY, l_run = 0.f;
+      // Fixed shift (maxdiffusion PR #477, "fixed-m"), when the caller passes score bounds: a row
+      // whose bound U >= |z| (log2 units, Cauchy-Schwarz: |q| max|k| scale log2 e) passes the gate
+      // floor((C + 125) / 2), C = 127 - ceil(log2 n) - ceil(log2 256) for the split's n keys, with
+      // every |v| <= 256, takes its weights as 2^(z - m) with m = ceil(U) - C fixed before the split is
+      // read: no running max, no rescale, and no term overflows or falls below 2^-125. Other rows keep
+      // the online max. P in f16 (the widened fp8 window) cannot hold 2^C: that path is never fixed.
+      bool fixed = false;
+      float m_fix = 0.f;
+      if (!PvF16 && p.fs_kv_max != nullptr && row_ok) {
+        const int64_t orow = (static_cast<int64_t>(mu.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mu.h) * G + gq;
+        const float2 kv = *reinterpret_cast<const float2*>(p.fs_kv_max + 2 * (static_cast<int64_t>(mu.b) * p.h_kv + mu.h));
+        const float U = p.fs_q_norm[orow] * kv.x * p.fs_scale_log2;
+        const int n_keys = max(mu.end - mu.start, 1);
+        const int Cn = 127 - (32 - __clz(n_keys - 1)) - 8;   // ceil(log2 n), ceil(log2 256) = 8
+        fixed = U <= static_cast<float>((Cn + 125) / 2) && kv.y <= 256.f;   // false for NaN bounds
+        m_fix = ceilf(U) - static_cast<float>(Cn);
+      }
+      float m_run = fixed ? m_fix : -INFINITY, l_run = 0.f;
       uint32_t pb = 0, pp = 0;   // buffer and phase count of the previous tile (g - 1)
       for (int t = 0; t < mu.tiles; ++t) {
         const int n0 = mu.start + t * kMmaN;
@@ -623,19 +640,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
           for (int j = 0; j < kMmaN; ++j) sr[j] = j <= lim ? sr[j] : 0xff800000u;   // -inf
         }
-        float mxa[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mxa[i] = __uint_as_float(sr[i]);
-#pragma unroll
-        for (int j = 8; j < kMmaN; ++j) mxa[j & 7] = max_nan(mxa[j & 7], __uint_as_float(sr[j]));
-#pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) mxa[i] = max_nan(mxa[i], mxa[i + w]);
         const float c = p.qk_scale_log2;
-        const float mx = mxa[0] * c;
+        float mx = -INFINITY;
+        if (!fixed) {
+          float mxa[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mxa[i] = __uint_as_float(sr[i]);
+#pragma unroll
+          for (int j = 8; j < kMmaN; ++j) mxa[j & 7] = max_nan(mxa[j & 7], __uint_as_float(sr[j]));
+#pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) mxa[i] = max_nan(mxa[i], mxa[i + w]);
+          mx = mxa[0] * c;
+        }
         // a NaN running max stays NaN (a later tile the row cannot see, max -inf, must not replace it)
-        const bool grow = !(mx <= m_run + kMmaTau) && m_run == m_run;
+        const bool grow = !fixed && !(mx <= m_run + kMmaTau) && m_run == m_run;
         const float m_new = grow ? mx : m_run;
         const float f = grow ? fast_exp2(m_run - m_new) : 1.f;
         if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
@@ -706,6 +726,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
       if (!ok) break;
+      if (fixed && l_run == 0.f) m_run = -INFINITY;   // no visible key: an empty partial, as online
       // ---- the unit's last PV is done: O is complete
       if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
         ok = false;

@@ -122,7 +122,17 @@ struct DecodeParams {
   // use); set only through nbx_set_decode_wait_test, to make a bounded wait run out on purpose
   uint64_t wait_limit_ns;
   uint64_t producer_delay_ns;
+  // fixed-shift softmax on the tensor-core kernel (null: the online max everywhere): per query vector
+  // |q| [batch * rows * h_q], per (sequence, KV head) {max |k| * k_scale, max |v| * v_scale}, and
+  // scale * log2(e)
+  const float* fs_q_norm;
+  const float* fs_kv_max;
+  float fs_scale_log2;
+  float k_scale_host;   // the pool's k scale (the bounds kernel reports |k| dequantised)
 };
+
+cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, float* q_norm, float* kv_max,
+                            cudaStream_t stream);
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);
 

@@ -2,6 +2,7 @@
 include/nbx.h, and refuses bad arguments on the host before any CUDA call."""
 
 import ctypes
+import json
 import os
 import re
 
@@ -209,3 +210,27 @@ def test_partial_kernel_choice(lib):
     assert lib.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 5, 256, 10, 64) == -2
     assert lib.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 256, 10, 40) == -4
     assert lib.nbx_paged_decode_partial_kernel(7, nbx.NBX_BF16, 16, 24, 4, 256, 10, 64) == -3
+
+
+def test_fixed_shift_constants_match_the_printed_examples(lib):
+    # maxdiffusion PR #477 prints C(N) and the gate for N = 4096 and N = 75,600 with Vmax = 256
+    with open(os.path.join(ROOT, "tests", "golden", "fixed_m_constants.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        assert nbx.nbx_decode_fixed_shift_gate(c["n_keys"], g["v_max_bound"]) == (c["C"], c["gate"])
+    # and the closed form at powers of two: C = 127 - log2 n - 8, gate = floor((C + 125) / 2)
+    for lg in range(0, 20):
+        C, gate = nbx.nbx_decode_fixed_shift_gate(1 << lg, 256.0)
+        assert C == 119 - lg and gate == (C + 125) // 2
+    with pytest.raises(nbx.NbxError):
+        nbx.nbx_decode_fixed_shift_gate(0, 256.0)
+
+
+def test_fixed_shift_entry_points_refuse_missing_bounds(lib):
+    f = lib.nbx_paged_decode_attn_fixed_shift
+    st = f(FAKE, 1, 2, 16, 8, 128, FAKE, FAKE, 1, 100, 2, 64, FAKE, 10, FAKE, 160, 0.1, 1.0, 1.0, FAKE, FAKE, 1 << 30,
+           NULL, FAKE, NULL, NULL)
+    assert st == -1
+    st = lib.nbx_paged_decode_bounds(FAKE, 1, 2, 16, 8, 128, FAKE, FAKE, 1, 100, 2, 64, FAKE, 10, FAKE, 160, 1.0, 0.0,
+                                     FAKE, FAKE, NULL, NULL)
+    assert st == -8   # v_scale 0
