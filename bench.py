@@ -371,6 +371,41 @@ def pack_inputs(sess, dev):
     return dev_buf, host_buf, total
 
 
+def time_fixed_shift(sess, steps: int, flush, sink, stream):
+    """The fixed-shift ablation of a tensor-core window: its bounds pass and the decode call with the
+    bounds (precomputed outside the timed decode), each timed like the decode call."""
+    import paged_split_kv_append_gb300 as nbx
+    with torch.cuda.stream(stream):
+        qn, kv = nbx.nbx_paged_decode_bounds(sess.q, sess.k_pool, sess.v_pool, sess.block_table, sess.seq_lens,
+                                             sess.max_seq_len, sess.k_scale, sess.v_scale, status=sess.status,
+                                             stream=stream)
+
+        def fixed():
+            nbx.nbx_paged_decode_attn_fixed_shift(sess.q, sess.k_pool, sess.v_pool, sess.block_table, sess.seq_lens,
+                                                  sess.max_seq_len, sess.scale, qn, kv, sess.k_scale, sess.v_scale,
+                                                  out=sess.out, workspace=sess.workspace, status=sess.status,
+                                                  stream=stream)
+
+        def bounds():
+            nbx.nbx_paged_decode_bounds(sess.q, sess.k_pool, sess.v_pool, sess.block_table, sess.seq_lens,
+                                        sess.max_seq_len, sess.k_scale, sess.v_scale, status=sess.status,
+                                        stream=stream)
+        out = {}
+        for name, fn in (("fixed_shift_decode_us", fixed), ("bounds_us", bounds)):
+            fn()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for a, b in evs:
+                flush_l2(flush, sink)
+                a.record(stream)
+                fn()
+                b.record(stream)
+            stream.synchronize()
+            out[name] = round(sum(a.elapsed_time(b) for a, b in evs) / steps * 1e3, 3)
+    if sess.status_bits() != 0:
+        raise RuntimeError(f"device status {sess.status_bits():#x} after the fixed-shift ablation")
+    return out
+
+
 def time_case(case, dev, steps: int, warmup: int, flush, sink, stream, e2e_steps: int = 0):
     """Time one workload's step (a CUDA-graph replay of append + decode) and its decode call alone
     (plan + partial + merge, eager), each with the L2 flushed before every timed iteration; with
@@ -411,6 +446,8 @@ def time_case(case, dev, steps: int, warmup: int, flush, sink, stream, e2e_steps
     step_launches = decode_launches + (1 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 0)
     r = dict(step_ms=step_ms, ms_per_step=sum(step_ms) / len(step_ms), dec_ms=sum(dec_ms) / len(dec_ms),
              launches=(step_launches + decode_launches) * steps, partial=partial_kernel_name(case.cfg))
+    if "mma" in r["partial"] and not e2e_steps:
+        r["fixed_shift"] = time_fixed_shift(sess, steps, flush, sink, stream)
     if e2e_steps:
         # end to end: one H2D copy of the step's packed inputs from pinned memory, the step through
         # the public API, one D2H copy of the output, per step
@@ -496,6 +533,11 @@ def run_gpu(args, rank: int, world: int):
                          "decode_us": round(rr["dec_ms"] * 1e3, 3), "kv_bytes": int(c.kv_bytes()),
                          "roofline": {**roof, "traffic": profiled_traffic(name, c.kv_bytes())},
                          "clocks": clk.summary()}
+            if "fixed_shift" in rr:
+                per[name]["fixed_shift_ablation"] = {
+                    **rr["fixed_shift"],
+                    "what": "decode call with the fixed-shift softmax (maxdiffusion PR #477) where the score bound "
+                            "passes the gate, bounds precomputed; bounds_us is the pass that computes them"}
             if name in CONTEXT:
                 per[name]["context"] = CONTEXT[name]
             del c

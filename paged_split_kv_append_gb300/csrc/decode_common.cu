@@ -343,28 +343,35 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
 
 // ------------------------------------------------------------------------------------ score bounds
 constexpr int kBoundsThreads = 256;
+constexpr int kBoundsChunk = 512;   // positions per CTA
 
 // Score bounds for the fixed-shift softmax (maxdiffusion PR #477: the metadata computed before the
 // kernel, here per query vector and per (sequence, KV head)): |q| of every query vector, and
 // max_j |k_j| * k_scale and max_{j,d} |v_jd| * v_scale over the positions a sequence holds, read
 // through the block table. A NaN input gives a NaN bound, which no gate passes; a length out of
 // bounds is read as empty (NBX_DEV_BAD_LEN) and a page id outside the pool is skipped
-// (NBX_DEV_BAD_PAGE). One CTA per (sequence, KV head), a warp per position; the CTAs of KV head 0
-// also write the sequence's query norms.
+// (NBX_DEV_BAD_PAGE). One CTA per (sequence, KV head, chunk of 512 positions), a warp per position;
+// the chunks combine with an atomic max on the bit patterns (the bounds are >= 0, and a NaN's bits
+// order above every finite value's), so kv_max must hold zeros first. The chunk-0 CTAs of KV head 0
+// write the sequence's query norms.
 template <class PT, class QT>
-__global__ void __launch_bounds__(kBoundsThreads) bounds_kernel(DecodeParams p, float* q_norm, float* kv_max) {
+__global__ void __launch_bounds__(kBoundsThreads) bounds_kernel(DecodeParams p, float* q_norm, float* kv_max,
+                                                                 int n_chunks) {
   __shared__ float s_k[kBoundsThreads / 32], s_v[kBoundsThreads / 32];
-  const int b = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.h_kv));
-  const int h = static_cast<int>(blockIdx.x - static_cast<unsigned>(b) * p.h_kv);
+  const int chunk = static_cast<int>(blockIdx.x % static_cast<unsigned>(n_chunks));
+  const int bh = static_cast<int>(blockIdx.x / static_cast<unsigned>(n_chunks));   // b * h_kv + h
+  const int b = bh / p.h_kv;
+  const int h = bh - b * p.h_kv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kWarps = kBoundsThreads / 32;
   int L = p.seq_lens[b];
   if (L < 0 || L > p.max_seq_len || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_pages) * p.page_tokens) {
-    if (h == 0 && threadIdx.x == 0) raise_status(p.status, NBX_DEV_BAD_LEN);
+    if (h == 0 && chunk == 0 && threadIdx.x == 0) raise_status(p.status, NBX_DEV_BAD_LEN);
     L = 0;
   }
+  const int j0 = chunk * kBoundsChunk, j1 = min(L, j0 + kBoundsChunk);
   float k2 = 0.f, va = 0.f;   // max |k|^2 and max |v| (pool units) over this warp's positions
-  for (int j = warp; j < L; j += kWarps) {
+  for (int j = j0 + warp; j < j1; j += kWarps) {
     const int page = p.block_table[static_cast<int64_t>(b) * p.max_pages + j / p.page_tokens];
     if (page < 0 || page >= p.num_pages) {
       if (lane == 0) raise_status(p.status, NBX_DEV_BAD_PAGE);
@@ -393,16 +400,16 @@ __global__ void __launch_bounds__(kBoundsThreads) bounds_kernel(DecodeParams p, 
     s_v[warp] = va;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && j0 < L) {
     float kt = 0.f, vt = 0.f;
     for (int w = 0; w < kWarps; ++w) {
       kt = max_nan(kt, s_k[w]);
       vt = max_nan(vt, s_v[w]);
     }
-    kv_max[2 * blockIdx.x] = sqrtf(kt) * p.k_scale_host;
-    kv_max[2 * blockIdx.x + 1] = vt * p.v_scale;
+    atomicMax(reinterpret_cast<int*>(kv_max) + 2 * bh, __float_as_int(sqrtf(kt) * p.k_scale_host));
+    atomicMax(reinterpret_cast<int*>(kv_max) + 2 * bh + 1, __float_as_int(vt * p.v_scale));
   }
-  if (h != 0) return;
+  if (h != 0 || chunk != 0) return;
   const int nq = p.rows * p.h_q;   // this sequence's query vectors
   for (int v = warp; v < nq; v += kWarps) {
     const char* qr = static_cast<const char*>(p.q) + (static_cast<int64_t>(b) * nq + v) * p.d * QT::kBytes;
@@ -419,16 +426,21 @@ __global__ void __launch_bounds__(kBoundsThreads) bounds_kernel(DecodeParams p, 
 
 cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, float* q_norm, float* kv_max,
                             cudaStream_t stream) {
-  const unsigned grid = static_cast<unsigned>(p.batch * p.h_kv);
+  cudaError_t e = cudaMemsetAsync(kv_max, 0, static_cast<size_t>(p.batch) * p.h_kv * 2 * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int n_chunks = p.max_seq_len > 0 ? (p.max_seq_len + kBoundsChunk - 1) / kBoundsChunk : 1;
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(p.batch) * p.h_kv * n_chunks);
+#define NBX_BOUNDS(PT, QT) bounds_kernel<PT, QT><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max, n_chunks)
   if (q_dtype == NBX_F32) {
-    if (pool_dtype == NBX_F32) bounds_kernel<F32, F32><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
-    else if (pool_dtype == NBX_BF16) bounds_kernel<BF16, F32><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
-    else bounds_kernel<E4M3, F32><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+    if (pool_dtype == NBX_F32) NBX_BOUNDS(F32, F32);
+    else if (pool_dtype == NBX_BF16) NBX_BOUNDS(BF16, F32);
+    else NBX_BOUNDS(E4M3, F32);
   } else {
-    if (pool_dtype == NBX_F32) bounds_kernel<F32, BF16><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
-    else if (pool_dtype == NBX_BF16) bounds_kernel<BF16, BF16><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
-    else bounds_kernel<E4M3, BF16><<<grid, kBoundsThreads, 0, stream>>>(p, q_norm, kv_max);
+    if (pool_dtype == NBX_F32) NBX_BOUNDS(F32, BF16);
+    else if (pool_dtype == NBX_BF16) NBX_BOUNDS(BF16, BF16);
+    else NBX_BOUNDS(E4M3, BF16);
   }
+#undef NBX_BOUNDS
   return cudaGetLastError();
 }
 
