@@ -53,6 +53,9 @@ __device__ __forceinline__ void store4<E4M3>(void* p, float4 v) {
 
 template <class In, class Out>
 __global__ void __launch_bounds__(256) append_kernel(AppendParams p) {
+  // a decode launched next may start its plan now: the plan reads only the lengths and waits for
+  // this grid before it writes any of them, and the decode's own kernels wait for the plan
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;

@@ -55,6 +55,15 @@ bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq
   return true;
 }
 
+// The plan kernel may run while the kernel before it (a decode step's append, which reads the
+// lengths) still runs: it waits for that grid before the step's length advance, and before it
+// completes, so the kernels after it see the append's positions.
+__device__ __forceinline__ void plan_finish(const DecodeParams& p) {
+  pdl_wait();
+  if (p.lens_out)   // the step's length advance; nothing later reads seq_lens
+    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) p.lens_out[b] = p.seq_lens[b] + p.len_add;
+}
+
 // Reads the device lengths, writes every sequence's plan (len, positions per split, non-empty
 // splits), zeroes the work counter, writes 0 to the output rows of empty sequences, and writes
 // the work list of (sequence, split) entries: sequences with the longest splits first (stable),
@@ -81,7 +90,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   for (int b = tid; b < B; b += kPlanThreads) {
     int L = p.seq_lens[b] + p.len_add;   // a decode step attends to its own new positions
     if (p.ident_bt) p.ident_bt[b] = b;
-    if (p.lens_out) p.lens_out[b] = L;   // the step's length advance; nothing later reads seq_lens
     if (L < 0 || L > p.max_seq_len || static_cast<int64_t>(L) > cap) {
       raise_status(p.status, NBX_DEV_BAD_LEN);
       L = 0;
@@ -134,6 +142,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
       }
       p.header[0] = base;
     }
+    plan_finish(p);
     return;
   }
   // stable rank by split length, longest first (empty sequences last)
@@ -196,6 +205,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
     p.entries[e] = en;
   }
   if (tid == 0) p.header[0] = total;
+  plan_finish(p);
 }
 
 // ------------------------------------------------------------------------------------ standalone merge
@@ -446,8 +456,7 @@ cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit,
                             cudaStream_t stream) {
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(plan_kernel, 1u, kPlanThreads, 0, stream, p);
   if (e != cudaSuccess) return e;
   if (p.widen_k != nullptr) e = decode_dispatch_widened(p, grid_limit, stream);
   else if (mma_path_applies(p, q_dtype, pool_dtype)) e = decode_dispatch_mma(p, grid_limit, stream);
