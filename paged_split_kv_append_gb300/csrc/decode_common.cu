@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   __shared__ int s_base[kSortMax + 1];
   __shared__ int s_warp[kPlanThreads / 32];
   __shared__ int s_empty;
+  __shared__ int s_nb;
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int B = p.batch;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   pdl_launch_dependents();   // the partial kernel may start its prologue now; it waits for this grid
   if (tid == 0) {
     s_empty = 0;
+    s_nb = 0;
     p.header[1] = 0;
   }
   __syncthreads();
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
     // kept in L2 for the merge, which reads the split counts after the K/V stream
     st_global_hint(reinterpret_cast<int4*>(p.plan + b), make_int4(L, seg, n, 0), l2_evict_last_policy());
     if (n == 0) s_empty = 1;
+    else if (small) atomicAdd(&s_nb, 1);
     if (small) {
       s_len[b] = L;
       s_seg[b] = seg;
@@ -145,7 +148,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
     plan_finish(p);
     return;
   }
-  // stable rank by split length, longest first (empty sequences last)
+  // stable rank by split length, longest first (empty sequences last). The list then holds every
+  // sequence's last split first (in that order), then the other splits: the last splits are of
+  // uneven length, so the persistent grid's first wave of units ends at scattered times instead of
+  // every CTA reaching a unit boundary at once; the rest follow longest first.
   for (int b = tid; b < B; b += kPlanThreads) {
     const int k = s_n[b] > 0 ? s_seg[b] : -1;
     int rank = 0;
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   const int per = (B + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(B, tid * per), hi = min(B, lo + per);
   int run = 0;
-  for (int i = lo; i < hi; ++i) run += s_n[s_order[i]];
+  for (int i = lo; i < hi; ++i) run += max(s_n[s_order[i]] - 1, 0);
   int x = run;
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -180,20 +186,28 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   int base = x - run + (warp > 0 ? s_warp[warp - 1] : 0);
   for (int i = lo; i < hi; ++i) {
     s_base[i] = base;
-    base += s_n[s_order[i]];
+    base += max(s_n[s_order[i]] - 1, 0);
   }
   if (tid == kPlanThreads - 1) s_base[B] = x + (warp > 0 ? s_warp[warp - 1] : 0);
   __syncthreads();
   // the entries, in parallel: entry e belongs to the list position i with s_base[i] <= e < s_base[i+1]
-  const int total = s_base[B];
+  const int nb = s_nb;
+  const int total = s_base[B] + nb;
   for (int e = tid; e < total; e += kPlanThreads) {
-    int l = 0, r = B - 1;
-    while (l < r) {
-      const int m = (l + r + 1) >> 1;
-      if (s_base[m] <= e) l = m; else r = m - 1;
+    int b, s;
+    if (e < nb) {
+      b = s_order[e];
+      s = s_n[b] - 1;
+    } else {
+      const int e2 = e - nb;
+      int l = 0, r = B - 1;
+      while (l < r) {
+        const int m = (l + r + 1) >> 1;
+        if (s_base[m] <= e2) l = m; else r = m - 1;
+      }
+      b = s_order[l];
+      s = e2 - s_base[l];
     }
-    const int b = s_order[l];
-    const int s = e - s_base[l];
     Entry en;
     en.b = b;
     en.s = s;
