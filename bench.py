@@ -43,6 +43,7 @@ METRIC = "paged decode attn µs/step and KV-read GB/s (% of GB300 HBM peak)"
 DEFAULT_CONFIG = "single_row"
 KERNEL_SOURCES = ("paged_split_kv_append_gb300/csrc/decode_kernels.cuh",
                   "paged_split_kv_append_gb300/csrc/nbx_device.cuh",
+                  "paged_split_kv_append_gb300/csrc/nbx_tcgen05.cuh",
                   "paged_split_kv_append_gb300/csrc/decode_common.cu",
                   "paged_split_kv_append_gb300/csrc/decode_mma.cu")
 
