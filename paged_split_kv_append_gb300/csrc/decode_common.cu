@@ -1,5 +1,7 @@
 // The split plan kernel, the standalone merge kernel, the workspace layout and the
 // decode launch sequence (plan, then the persistent partial kernel).
+#include <cuda_fp16.h>
+
 #include "decode_kernels.cuh"
 
 namespace nbx {
@@ -278,6 +280,8 @@ constexpr int kDecodeMergeThreads = 32;   // one warp per CTA
 // reductions, a fixed order), the weights reach every lane by shuffles, and each lane owns one
 // float4 of the output, with every split's accumulator load in flight and the sum in ascending
 // split order.
+// F16: the partials are f16 acc / l (DecodeParams::part_f16); a split then weighs 2^(m - M) * l.
+template <bool F16>
 __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(DecodeParams p) {
   const int lane = threadIdx.x;
   const int RG = p.rows * p.group;
@@ -311,10 +315,21 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
     const float* m = p.m_part + orow * p.max_splits;
     const float* l = p.l_part + orow * p.max_splits;
     const float4* acc = reinterpret_cast<const float4*>(p.acc_part + orow * p.max_splits * p.d);
+    // f16 partials: the d halves at the start of each split's d-float slot, 4 per lane (8 bytes)
+    const uint2* acc_h = reinterpret_cast<const uint2*>(p.acc_part + orow * p.max_splits * p.d);
     auto load_batch = [&](int j, int s0, float4 (&a)[32]) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k)
-        a[k] = (j < d4 && s0 + k < S) ? acc[static_cast<int64_t>(s0 + k) * d4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < 32; ++k) {
+        const bool in = j < d4 && s0 + k < S;
+        if constexpr (F16) {
+          const uint2 hv = in ? acc_h[static_cast<int64_t>(s0 + k) * (2 * d4) + j] : make_uint2(0u, 0u);
+          const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
+          const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
+          a[k] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        } else {
+          a[k] = in ? acc[static_cast<int64_t>(s0 + k) * d4 + j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
     };
     float4 a[32];
     load_batch(j, 0, a);   // in flight together with the m / l loads
@@ -336,7 +351,8 @@ __global__ void __launch_bounds__(kDecodeMergeThreads) decode_merge_kernel(Decod
     for (int k = 0; k < 2; ++k) {
       const float w = live[k] ? fast_exp2(mv[k] - M) : 0.f;
       if (live[k]) L += w * lv[k];
-      wv[k] = live[k] ? w : -1.f;
+      // an f16 partial is acc / l: its weight carries l
+      wv[k] = live[k] ? (F16 ? w * lv[k] : w) : -1.f;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -472,17 +488,21 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
                             cudaStream_t stream) {
   cudaError_t e = launch_pdl(plan_kernel, 1u, kPlanThreads, 0, stream, p);
   if (e != cudaSuccess) return e;
-  if (p.widen_k != nullptr) e = decode_dispatch_widened(p, grid_limit, stream);
-  else if (mma_path_applies(p, q_dtype, pool_dtype)) e = decode_dispatch_mma(p, grid_limit, stream);
-  else if (pool_dtype == NBX_F32) e = decode_dispatch_F32(p, q_dtype, grid_limit, stream);
-  else if (pool_dtype == NBX_BF16) e = decode_dispatch_BF16(p, q_dtype, grid_limit, stream);
-  else e = decode_dispatch_E4M3(p, q_dtype, grid_limit, stream);
+  DecodeParams q = p;
+  q.part_f16 = p.widen_k != nullptr ? 1 : 0;   // fp8 windows on tensor cores: f16 partials
+  if (q.widen_k != nullptr) e = decode_dispatch_widened(q, grid_limit, stream);
+  else if (mma_path_applies(q, q_dtype, pool_dtype)) e = decode_dispatch_mma(q, grid_limit, stream);
+  else if (pool_dtype == NBX_F32) e = decode_dispatch_F32(q, q_dtype, grid_limit, stream);
+  else if (pool_dtype == NBX_BF16) e = decode_dispatch_BF16(q, q_dtype, grid_limit, stream);
+  else e = decode_dispatch_E4M3(q, q_dtype, grid_limit, stream);
   if (e != cudaSuccess) return e;
-  if (p.max_splits <= 1) return cudaSuccess;   // every sequence has one split: the partials are the output
-  const int64_t items = static_cast<int64_t>(p.batch) * p.h_kv * p.row_blocks * kQB * ((p.d / 4 + 31) / 32);
+  if (q.max_splits <= 1) return cudaSuccess;   // every sequence has one split: the partials are the output
+  const int64_t items = static_cast<int64_t>(q.batch) * q.h_kv * q.row_blocks * kQB * ((q.d / 4 + 31) / 32);
   int64_t grid = static_cast<int64_t>(device_info().sm_count) * 24;
   if (grid > items) grid = items;
-  return launch_pdl(decode_merge_kernel, static_cast<unsigned>(grid), kDecodeMergeThreads, 0, stream, p);
+  if (q.part_f16)
+    return launch_pdl(decode_merge_kernel<true>, static_cast<unsigned>(grid), kDecodeMergeThreads, 0, stream, q);
+  return launch_pdl(decode_merge_kernel<false>, static_cast<unsigned>(grid), kDecodeMergeThreads, 0, stream, q);
 }
 
 }  // namespace nbx

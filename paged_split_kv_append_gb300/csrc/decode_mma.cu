@@ -627,6 +627,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       tc_fence_after();
       const bool single = mu.n_splits <= 1;
       const float sc = single ? ((m_run == -INFINITY) ? 0.f : p.v_scale / l_run) : 1.f;
+      // f16 partials (fp8 windows): acc / l, which stays within the E4M3 codes' range
+      const bool half_part = PvF16 && p.part_f16 && !single;
+      const float il = (m_run == -INFINITY) ? 0.f : 1.f / l_run;
       float* dst = nullptr;
       if (row_ok) {
         const int64_t orow = (static_cast<int64_t>(mu.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mu.h) * G + gq;
@@ -646,7 +649,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           tc_fence_before();
           mbar_arrive(o_free);
         }
-        if (dst != nullptr) {
+        if (dst != nullptr && half_part) {
+          // 32 halves: two 32-byte stores into the first half of the split's slot
+#pragma unroll
+          for (int c16 = 0; c16 < kChunk / 16; ++c16) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const __half2 h = __floats2half2_rn(__uint_as_float(ov[16 * c16 + 2 * e]) * il,
+                                                  __uint_as_float(ov[16 * c16 + 2 * e + 1]) * il);
+              v[e] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h));
+            }
+            st_global_v8_hint(dst + (ch * kChunk) / 2 + c16 * 8, v, keep);   // kept in L2 for the merge
+          }
+        } else if (dst != nullptr) {
 #pragma unroll
           for (int c8 = 0; c8 < kChunk / 8; ++c8) {
             float v[8];

@@ -129,6 +129,11 @@ struct DecodeParams {
   const float* fs_kv_max;
   float fs_scale_log2;
   float k_scale_host;   // the pool's k scale (the bounds kernel reports |k| dequantised)
+  // split partials as f16 acc / l (the partial normalised by its own sum) instead of fp32 acc: set
+  // for fp8 windows on tensor cores, where acc / l is a convex combination of E4M3 codes (|code|
+  // <= 448, the v scale is applied by the merge), so f16 neither overflows nor loses more than
+  // 2^-11 relative; each (row, split) slot holds d halves in the first half of its d floats
+  int part_f16;
 };
 
 cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, float* q_norm, float* kv_max,
