@@ -70,6 +70,9 @@ __device__ __forceinline__ void plan_finish(const DecodeParams& p) {
 // splits), zeroes the work counter, writes 0 to the output rows of empty sequences, and writes
 // the work list of (sequence, split) entries: sequences with the longest splits first (stable),
 // splits ascending. Batches above kSortMax keep their own order and take a slower serial path.
+// TC: a tensor-core window, whose splits are sized by the call's total work (DecodeParams::tc_units);
+// otherwise the pages' rule. Two instantiations keep the pages' rule's code free of the other.
+template <bool TC>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   __shared__ int s_len[kSortMax];
   __shared__ int s_seg[kSortMax];
@@ -85,12 +88,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   const int64_t cap = static_cast<int64_t>(p.max_pages) * p.page_tokens;
   const bool small = B <= kSortMax;
   pdl_launch_dependents();   // the partial kernel may start its prologue now; it waits for this grid
+  __shared__ long long s_total;
   if (tid == 0) {
     s_empty = 0;
     s_nb = 0;
+    if constexpr (TC) s_total = 0;
     p.header[1] = 0;
   }
   __syncthreads();
+  // a tensor-core window sizes its splits by the whole call's work: the sum of the lengths
+  long long len_sum = 0;
+  if constexpr (TC) {
+    long long part = 0;
+    for (int b = tid; b < B; b += kPlanThreads) {
+      const int L = p.seq_lens[b] + p.len_add;
+      if (L > 0 && L <= p.max_seq_len && static_cast<int64_t>(L) <= cap) part += L;
+    }
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0 && part) atomicAdd(reinterpret_cast<unsigned long long*>(&s_total), static_cast<unsigned long long>(part));
+    __syncthreads();
+    len_sum = s_total;
+  }
   for (int b = tid; b < B; b += kPlanThreads) {
     int L = p.seq_lens[b] + p.len_add;   // a decode step attends to its own new positions
     if (p.ident_bt) p.ident_bt[b] = b;
@@ -98,8 +116,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
       raise_status(p.status, NBX_DEV_BAD_LEN);
       L = 0;
     }
-    int S = (max(L, 1) + NBX_SPLIT_POSITIONS - 1) / NBX_SPLIT_POSITIONS;
-    S = S > NBX_MAX_SPLITS ? NBX_MAX_SPLITS : S;
+    int S;
+    if (TC && len_sum > 0) {
+      // about tc_units units in all, shared in proportion to the lengths (the grid's one wave); a
+      // split keeps at least 64 positions (the tensor-core tile), and a sequence has at most the
+      // workspace's partial slots (max_splits, the pages' rule at the longest length)
+      const long long want = static_cast<long long>(p.tc_units) * L / (static_cast<long long>(p.tc_pairs) * len_sum);
+      const int cap_s = min(p.max_splits, max(1, L / 64));
+      S = static_cast<int>(want < 1 ? 1 : (want > cap_s ? cap_s : want));
+    } else {
+      S = (max(L, 1) + NBX_SPLIT_POSITIONS - 1) / NBX_SPLIT_POSITIONS;
+      S = S > NBX_MAX_SPLITS ? NBX_MAX_SPLITS : S;
+    }
     int seg = (L + S - 1) / S;
     // splits start on whole pages, or on 256-position boundaries when a page is longer (a
     // contiguous cache read as one page per sequence): tile starts either way
@@ -486,10 +514,18 @@ cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit,
                             cudaStream_t stream) {
-  cudaError_t e = launch_pdl(plan_kernel, 1u, kPlanThreads, 0, stream, p);
-  if (e != cudaSuccess) return e;
   DecodeParams q = p;
   q.part_f16 = p.widen_k != nullptr ? 1 : 0;   // fp8 windows on tensor cores: f16 partials
+  if (p.widen_k != nullptr || mma_path_applies(p, q_dtype, pool_dtype)) {
+    // a tensor-core window: splits sized for one wave of work units over the GPU's SMs (the grid
+    // limit does not enter, so the partition, and the result, is the same at any grid size)
+    const int rt = p.rows < kMmaRowsPerTile / p.group ? p.rows : kMmaRowsPerTile / p.group;
+    q.tc_units = device_info().sm_count;
+    q.tc_pairs = p.h_kv * ((p.rows + rt - 1) / rt);
+  }
+  cudaError_t e = q.tc_units > 0 ? launch_pdl(plan_kernel<true>, 1u, kPlanThreads, 0, stream, q)
+                                 : launch_pdl(plan_kernel<false>, 1u, kPlanThreads, 0, stream, q);
+  if (e != cudaSuccess) return e;
   if (q.widen_k != nullptr) e = decode_dispatch_widened(q, grid_limit, stream);
   else if (mma_path_applies(q, q_dtype, pool_dtype)) e = decode_dispatch_mma(q, grid_limit, stream);
   else if (pool_dtype == NBX_F32) e = decode_dispatch_F32(q, q_dtype, grid_limit, stream);

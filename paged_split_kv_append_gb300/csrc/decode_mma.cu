@@ -53,6 +53,7 @@ namespace nbx {
 namespace {
 
 constexpr int kMmaM = 128;       // TMEM lanes / rows of an M tile
+static_assert(kMmaM == kMmaRowsPerTile, "the plan's M tiles");
 constexpr int kMmaN = 64;        // positions per K/V tile
 constexpr int kMmaThreads = 256;
 constexpr int kSoftmaxThreads = 128;

@@ -134,6 +134,12 @@ struct DecodeParams {
   // <= 448, the v scale is applied by the merge), so f16 neither overflows nor loses more than
   // 2^-11 relative; each (row, split) slot holds d halves in the first half of its d floats
   int part_f16;
+  // split plan for a tensor-core window (0: the pages' rule, ceil(len / 256) splits of at most 64):
+  // about tc_units work units in all, each of the tc_pairs (KV head, M tile) pairs of a sequence
+  // taking floor(tc_units * len / (tc_pairs * sum of lens)) splits, clamped to [1, min(max_splits,
+  // len / 64)]
+  int tc_units;
+  int tc_pairs;
 };
 
 cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, float* q_norm, float* kv_max,
@@ -145,6 +151,7 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
 // (rows x group >= 64), q and pools are bf16, d is 128 or 256 and pages hold a multiple of 64
 // positions.
 bool mma_path_applies(const DecodeParams& p, int q_dtype, int pool_dtype);
+constexpr int kMmaRowsPerTile = 128;   // query vectors of one M tile of the tensor-core kernel
 cudaError_t decode_dispatch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream);
 
 // fp8 pools with a multi-row window: the same tensor-core kernel runs on bf16 copies of the
