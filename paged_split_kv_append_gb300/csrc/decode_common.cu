@@ -519,9 +519,8 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
   if (p.widen_k != nullptr || mma_path_applies(p, q_dtype, pool_dtype)) {
     // a tensor-core window: splits sized for one wave of work units over the GPU's SMs (the grid
     // limit does not enter, so the partition, and the result, is the same at any grid size)
-    const int rt = p.rows < kMmaRowsPerTile / p.group ? p.rows : kMmaRowsPerTile / p.group;
     q.tc_units = device_info().sm_count;
-    q.tc_pairs = p.h_kv * ((p.rows + rt - 1) / rt);
+    q.tc_pairs = p.h_kv * ((p.rows * p.group + kMmaRowsPerTile - 1) / kMmaRowsPerTile);
   }
   cudaError_t e = q.tc_units > 0 ? launch_pdl(plan_kernel<true>, 1u, kPlanThreads, 0, stream, q)
                                  : launch_pdl(plan_kernel<false>, 1u, kPlanThreads, 0, stream, q);

@@ -9,9 +9,9 @@
 // describes for its attn_rows kernel: each K/V tile is read once for all rows of a stream.
 //
 // GB300 design (one CTA per SM, 8 warps):
-//  * Work unit = (split entry, KV head, M tile), M tile fastest. An M tile holds Rt whole query
-//    rows x the G query heads of the KV head (Rt = min(rows, 128 / G)), so its Q block is a box
-//    of a 4-D tensor map. Static round-robin over the plan's longest-first list.
+//  * Work unit = (split entry, KV head, M tile), M tile fastest. The query vectors of one KV head,
+//    v = row * G + head, are cut into M tiles of 128 (a tile may split one row's heads), so no tile
+//    row is padding but in the last tile. Static round-robin over the plan's longest-first list.
 //  * Shared memory: the unit's Q tile (128-byte-swizzled K-major atoms of 64 columns), a K ring and
 //    a V ring of 16 KB slots (64 positions x 128 columns: half of a d=256 tile, a whole d=128
 //    tile; a tile is one page or a 64-aligned part of one). Every slot has a full barrier (TMA bytes) and an empty barrier (its consumer).
@@ -23,8 +23,9 @@
 //    two tiles ahead of PV.
 //  * Two issuing threads share the tensor pipe, each a plain sequence of bounded waits and MMAs
 //    (kind::f16, bf16 x bf16 -> fp32 in TMEM, completions signalled with tcgen05.commit):
-//      warp 5:  S[x % 3] = Q K(x)^T   M=128, N=64, K=d; Q and K from shared memory; it also loads
-//               each unit's Q tile by TMA once the previous unit's last QK^T has completed
+//      warp 5:  S[x % 3] = Q K(x)^T   M=128, N=64, K=d; Q and K from shared memory; its lanes 1-31
+//               copy each unit's Q tile (16-byte cp.async into the swizzled atoms, zeros past the
+//               last vector) once the previous unit's last QK^T has completed
 //      warp 7:  O += P_hi(y) V(y) + P_lo(y) V(y)   M=128, N=d (both V halves in one MMA), K=64;
 //               P from TMEM. It zeroes V rows past a split's end before their PV (0 x NaN would
 //               otherwise leak) and skips 16-position steps that hold none.
@@ -83,9 +84,16 @@ struct MmaCfg {
   static_assert(kHalves == 1 || (kVSlots % kHalves) == 0, "V ring length");
 };
 
+// Query rows per M tile when every tile holds whole rows (one tile, or a group dividing 128: the Q
+// tile is then one tensor box of the rows), else 0 (tiles split a row's heads; Q is copied by lanes).
+__host__ __device__ inline int whole_row_tile_rows(int rows, int group) {
+  if (rows * group <= kMmaM) return rows;
+  return (kMmaM % group) == 0 ? kMmaM / group : 0;
+}
+
 struct MmaMaps {
   CUtensorMap k, v;   // 2-D pool views [num_pages * h_kv * page_tokens][d], box 64 x 64
-  CUtensorMap q;      // 4-D [batch][rows][h_q][d] bf16, box {64, G, Rt, 1}
+  CUtensorMap q;      // 4-D [batch][rows][h_q][d] bf16, box {64, G, rows per tile, 1} (whole-row tiles)
 };
 
 // Bounded wait that also gives up when another role of the CTA has given up.
@@ -230,7 +238,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   constexpr int NK = C::kKSlots;
   constexpr int NV = C::kVSlots;
   constexpr int HI = C::kHalves;
-  constexpr int QA = D / 64;            // Q atoms
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   char* q_s = smem + C::kQOff;
@@ -245,7 +252,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   uint64_t* p_full = s_full + kSBufs;  // [3]   P of the buffer's tile in TMEM (128 arrivals)
   uint64_t* sp_free = p_full + kSBufs; // [3]   PV of the buffer's tile done: buffer reusable, O
                                        //       holds every PV up to that tile
-  uint64_t* q_full = sp_free + kSBufs; //       the unit's Q tile landed (TMA bytes)
+  uint64_t* q_full = sp_free + kSBufs; //       the unit's Q tile landed (the QK warp's lanes 1-31)
   uint64_t* q_empty = q_full + 1;      //       every QK^T of the unit done
   uint64_t* o_free = q_full + 2;       //       O read out by the epilogue (128 arrivals)
   uint64_t* done_bar = q_full + 3;     //       every PV of the CTA done
@@ -277,7 +284,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&sp_free[i], 1);
     }
-    mbar_init(q_full, 1);
+    // a tensor box (one arrival with the byte count) or the cp.async completions of lanes 1-31
+    mbar_init(q_full, whole_row_tile_rows(p.rows, p.group) > 0 ? 1 : 31);
     mbar_init(q_empty, 1);
     mbar_init(o_free, kSoftmaxThreads);
     mbar_init(done_bar, 1);
@@ -297,10 +305,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   pdl_launch_dependents();
 
   const int G = p.group;
-  const int Rt = min(p.rows, kMmaM / G);                 // query rows per M tile
-  const int m_tiles = (p.rows + Rt - 1) / Rt;
+  const int RG = p.rows * G;                             // query vectors of one KV head
+  const int m_tiles = (RG + kMmaM - 1) / kMmaM;          // M tiles of 128 of them
   const int n_units = p.header[0] * p.h_kv * m_tiles;
-  const uint32_t q_bytes = static_cast<uint32_t>(QA) * 64u * static_cast<uint32_t>(G * Rt) * 2u;
 
   if (warp == 4 || warp == 6) {
     // ======================================================== TMA producers, one warp per ring:
@@ -350,38 +357,23 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     __syncwarp();
   } else if (warp == 5) {
-    // ======================================================== QK^T issuer and Q loader (lane 0)
+    // ======================================================== QK^T issuer (lane 0), Q loader (lanes 1-31)
+    const uint32_t q_addr = smem_u32(q_s);
+    TileIter it;
+    it.begin(p, m_tiles, n_units, HI);
     if (lane == 0) {
       constexpr uint32_t kIdescS = mma_idesc(kMmaM, kMmaN, false);
-      const uint32_t q_addr = smem_u32(q_s);
-      TileIter it;
-      it.begin(p, m_tiles, n_units, HI);
       bool ok = true;
-      bool q_pending = false;     // a Q copy is in flight that no wait has seen land
       uint32_t sx = 0, sxp = 0;   // S/P buffer (x % 3) and its phase count (x / 3)
       while (!it.done) {
-        if (it.t == 0) {
-          // the unit's Q tile, once every QK^T of the previous unit has completed
-          if (it.k > 0 && !bwait(q_empty, (it.k - 1) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(q_full, q_bytes);
-#pragma unroll
-          for (int a = 0; a < QA; ++a)
-            tma_load_4d(q_s + a * (kMmaM * 128), &maps.q, a * 64, it.mu.h * G, it.mu.mt * Rt, it.mu.b, q_full);
-          q_pending = true;
-        }
         // S(x) = Q K(x)^T once the buffer's previous PV is done, K(x) has landed and the unit's Q has
         const uint32_t ki = it.item(it.t);
         if (it.x >= static_cast<uint32_t>(kSBufs)) ok = bwait(&sp_free[sx], (sxp - 1) & 1u, abort_flag);
         for (int j = 0; j < HI && ok; ++j) ok = bwait(&kfull[(ki + j) % NK], ((ki + j) / NK) & 1u, abort_flag);
-        if (ok && it.t == 0) {
-          ok = bwait(q_full, it.k & 1u, abort_flag);
-          q_pending = !ok;
-        }
+        if (ok && it.t == 0) ok = bwait(q_full, it.k & 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
+        if (it.t == 0) fence_proxy_async();   // Q was written by cp.async (generic proxy)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t a = kk >> 2, sub = kk & 3;   // 64-column atom, 16-column step in it
@@ -402,12 +394,65 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, NBX_DEV_TIMEOUT);
-        // a Q copy in flight has landed before the CTA exits
-        if (q_pending) mbar_wait(q_full, it.k & 1u, 100000000ull);
       }
       // every QK^T of this CTA has completed before the TMEM is released
       tc_commit(done_qk);
       mbar_wait(done_qk, 0, 100000000ull);
+    } else {
+      // Each unit's Q tile, once every QK^T of the previous unit has completed: vector i of the tile
+      // (v = 128 mt + i, row v / G, head v % G of the KV head) into row i of the 128-byte-swizzled
+      // K-major atoms, 16 bytes a copy; rows past the last vector are zero. These 31 lanes run apart
+      // from lane 0's MMA loop, meeting it only through the barriers.
+      constexpr unsigned kLoaders = 0xfffffffeu;
+      constexpr int kRowChunks = D / 8;   // 16-byte chunks per query vector
+      const int rt_box = whole_row_tile_rows(p.rows, G);   // > 0: the tile is one tensor box
+      bool ok = true;
+      for (uint32_t k = 0; !it.done; ++k) {
+        int r = 1;
+        if (lane == 1 && k > 0) r = bwait(q_empty, (k - 1) & 1u, abort_flag);
+        if (!__shfl_sync(kLoaders, r, 1)) {
+          ok = false;
+          break;
+        }
+        if (rt_box > 0) {   // whole rows: lane 1 loads the tile's rows as one box per 64-column atom
+          if (lane == 1) {
+            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>((D / 64) * 64 * G * rt_box * 2));
+#pragma unroll
+            for (int a = 0; a < D / 64; ++a)
+              tma_load_4d(q_s + a * (kMmaM * 128), &maps.q, a * 64, it.mu.h * G, it.mu.mt * rt_box, it.mu.b, q_full);
+          }
+          it.next_unit(p);
+          continue;
+        }
+        // lane l copies chunks l - 1, l + 30, ... of the tile: (vector i, chunk cc) and the vector's
+        // row and head, stepped without divisions
+        const int v0 = it.mu.mt * kMmaM;
+        int i = (lane - 1) / kRowChunks, cc = (lane - 1) % kRowChunks;
+        int v = v0 + i;
+        int rr = v / G, gg = v - rr * G;
+        const char* qb = static_cast<const char*>(p.q) +
+                         (static_cast<int64_t>(it.mu.b) * p.rows * p.h_q + static_cast<int64_t>(it.mu.h) * G) * (D * 2);
+        const int64_t row_stride = static_cast<int64_t>(p.h_q) * (D * 2);
+        while (i < kMmaM) {
+          const bool vq = v < RG;
+          const char* src = qb + rr * row_stride + gg * (D * 2) + cc * 16;
+          cp_async16_zfill(q_addr + (cc >> 3) * (kMmaM * 128) + i * 128 + (((cc & 7) ^ (i & 7)) << 4), vq ? src : qb, vq);
+          cc += 31;
+          while (cc >= kRowChunks) {
+            cc -= kRowChunks;
+            ++i;
+            ++v;
+            if (++gg == G) {
+              gg = 0;
+              ++rr;
+            }
+          }
+        }
+        cp_async_arrive_noinc(q_full);
+        it.next_unit(p);
+      }
+      cp_async_wait_all();   // this lane's Q copies have landed before the CTA exits
+      if (!ok && lane == 1) *abort_flag = 1;
     }
     __syncwarp();
   } else if (warp == 7) {
@@ -470,8 +515,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   } else {
     // ======================================================== softmax warps (row = threadIdx.x)
     const int row = threadIdx.x;
-    const int rt = row / G;                       // query row within the M tile
-    const int gq = row - rt * G;                  // query head within the KV head's group
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     // the split partials stay in L2 for the merge
     const uint64_t keep = l2_keep_policy(p.keep_frac);
@@ -483,8 +526,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     int pg_cur = it.done ? 0 : chunk_pages(p, it.mu, 0, lane), pg_nxt = 0;   // lane l: page of tile 32c + l
     while (!it.done && ok) {
       const MmaUnit mu = it.mu;
-      const int r = mu.mt * Rt + rt;
-      const bool row_ok = rt < Rt && r < p.rows;
+      const int vq = mu.mt * kMmaM + row;            // this thread's query vector of the KV head
+      const bool row_ok = vq < RG;
+      const int r = row_ok ? vq / G : 0;             // its query row
+      const int gq = row_ok ? vq - r * G : 0;        // its query head within the KV head's group
       const int pos = mu.len - p.rows + r;   // last position this row sees
       // Fixed shift (maxdiffusion PR #477, "fixed-m"), when the caller passes score bounds: a row
       // whose bound U >= |z| (log2 units, Cauchy-Schwarz: |q| max|k| scale log2 e) passes the gate
@@ -715,22 +760,22 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* ba
 
 bool make_maps(MmaMaps* m, const DecodeParams& p, bool v_f16) {
   const cuuint64_t D = static_cast<cuuint64_t>(p.d);
-  const cuuint32_t G = static_cast<cuuint32_t>(p.group);
-  const cuuint32_t Rt = static_cast<cuuint32_t>(p.rows < kMmaM / p.group ? p.rows : kMmaM / p.group);
-  const cuuint64_t R = static_cast<cuuint64_t>(p.rows), B = static_cast<cuuint64_t>(p.batch);
-  const cuuint64_t HQ = static_cast<cuuint64_t>(p.h_q);
   // pools: rows (page * h_kv + h) * page_tokens + position, columns d
   const cuuint64_t pool_dims[2] = {D, static_cast<cuuint64_t>(p.num_pages) * p.h_kv * p.page_tokens};
   const cuuint64_t pool_str[1] = {D * 2};
   const cuuint32_t pool_box[2] = {64, static_cast<cuuint32_t>(kMmaN)};
+  if (!encode(&m->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k_pool, pool_dims, pool_str, pool_box) ||
+      !encode(&m->v, v_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v_pool,
+              pool_dims, pool_str, pool_box))
+    return false;
+  const int rt = whole_row_tile_rows(p.rows, p.group);
+  if (rt == 0) return true;
   // q [B][R][h_q][d] bf16
-  const cuuint64_t q_dims[4] = {D, HQ, R, B};
+  const cuuint64_t HQ = static_cast<cuuint64_t>(p.h_q), R = static_cast<cuuint64_t>(p.rows);
+  const cuuint64_t q_dims[4] = {D, HQ, R, static_cast<cuuint64_t>(p.batch)};
   const cuuint64_t q_str[3] = {D * 2, HQ * D * 2, R * HQ * D * 2};
-  const cuuint32_t q_box[4] = {64, G, Rt, 1};
-  return encode(&m->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k_pool, pool_dims, pool_str, pool_box) &&
-         encode(&m->v, v_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v_pool,
-                pool_dims, pool_str, pool_box) &&
-         encode(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.q, q_dims, q_str, q_box);
+  const cuuint32_t q_box[4] = {64, static_cast<cuuint32_t>(p.group), static_cast<cuuint32_t>(rt), 1};
+  return encode(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.q, q_dims, q_str, q_box);
 }
 
 template <int D, bool PvF16>
@@ -748,8 +793,7 @@ cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t strea
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  const int Rt = p.rows < kMmaM / p.group ? p.rows : kMmaM / p.group;
-  const int m_tiles = (p.rows + Rt - 1) / Rt;
+  const int m_tiles = (p.rows * p.group + kMmaM - 1) / kMmaM;
   const int64_t upper = static_cast<int64_t>(p.batch) * p.max_splits * p.h_kv * m_tiles;
   int64_t grid = di.sm_count;
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;

@@ -261,6 +261,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src_gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src_gmem) : "memory");
 }
+// The same with a source size of 16 or 0 bytes: with `valid` false nothing is read (the source
+// address is not dereferenced) and the 16 destination bytes are zeroed.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst_smem, const void* src_gmem, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src_gmem), "r"(valid ? 16 : 0)
+               : "memory");
+}
 // Arrives on `bar` once every cp.async this thread issued before has completed; the arrival is one
 // of the barrier's expected arrivals (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
