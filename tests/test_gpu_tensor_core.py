@@ -198,3 +198,40 @@ def test_nan_key_reaches_rows_whose_later_tiles_are_masked():
     G = case.cfg.group
     assert np.all(np.isnan(want[0, :, G:2 * G]))
     assert pins.nan_aware_error(got, want) <= 3e-2
+
+
+def test_several_whole_row_query_tiles_per_head():
+    # 32 rows x group 8 = 256 query vectors: two M tiles of 16 whole rows each, so each tile's query
+    # block is one tensor box (the second at row 16); compared with the oracle and across grid sizes
+    cfg = tc_config("tc_whole_rows", 3, 32, 32, 4, 128, 64, ("uniform", 40, 3000), 39)
+    case = wl.make_case(cfg, device=DEV)
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+    for limit in (1, 5):
+        _, o2 = run_step(case, grid_limit=limit)
+        assert torch.equal(o2, out), f"grid limit {limit}"
+
+
+def test_fp8_window_partials_at_the_code_range_edge():
+    # An fp8 window stores each split's partial as f16 acc / l. Make every head attend almost
+    # entirely to one position whose value row holds the largest codes (+-448, the amax row that
+    # sets the v scale): the partials then sit at the edge of the E4M3 range, and the output must
+    # still match the oracle.
+    cfg = fp8_config("tc_fp8_edge", (2000, 1500), 40)
+    case = wl.make_case(cfg, device=DEV)
+    G = cfg.group
+    for b in range(cfg.batch):
+        off = int(case.tok_offset[b])
+        n = int(case.lens[b])
+        for h in range(cfg.h_kv):
+            pos = off + (37 * (h + 1) + 11 * b) % n
+            qv = case.q[b, :, h * G:(h + 1) * G].float().mean(dim=(0, 1))
+            case.k_raw[pos, h] = (8.0 * qv / qv.norm()).to(case.k_raw.dtype)
+            case.v_raw[pos, h] = torch.where(torch.arange(cfg.d, device=case.v_raw.device) % 2 == 0, 6.0, -6.0).to(
+                case.v_raw.dtype)
+    # the per-tensor scales follow the raw values (amax / 448)
+    case = wl.Case(**{**case.__dict__, "k_scale": float(case.k_raw.abs().max()) / wl.E4M3_MAX,
+                      "v_scale": float(case.v_raw.abs().max()) / wl.E4M3_MAX})
+    sess, out = run_step(case)
+    err = check_against_oracle(case, sess, out)
+    assert err <= 3e-2, err
