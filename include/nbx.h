@@ -127,10 +127,12 @@ NBX_API size_t nbx_paged_decode_workspace_bytes_for(int q_dtype, int pool_dtype,
  * p = seq_lens[b] - rows + r and attends keys 0..p of KV head h / (h_q / h_kv):
  *   s_j = scale * k_scale * (q . k_j),  out = v_scale * sum_j e^(s_j - max s) v_j / sum_j e^(s_j - max s).
  * A row with no visible key (p < 0, or seq_lens[b] == 0) gets 0. Each sequence is cut into
- * min(ceil(len/256), 64) splits of whole pages; each split's unnormalised partial (m, l, acc)
- * is computed with an fp32 online softmax and the partials are merged in ascending split order
- * (a split with m = -inf is skipped, so NaN inputs reach the output). The result does not
- * depend on the physical page ids or on the order the work runs in.
+ * min(ceil(len/256), 64) splits of whole pages (a window on tensor cores, see
+ * nbx_paged_decode_partial_kernel: about one work unit per SM in all, splits in proportion to the
+ * lengths, at most as many as the pages' rule gives at max_seq_len); each split's unnormalised
+ * partial (m, l, acc) is computed with an fp32 online softmax and the partials are merged in
+ * ascending split order (a split with m = -inf is skipped, so NaN inputs reach the output). The
+ * result does not depend on the physical page ids or on the order the work runs in.
  *
  *   q            [device] [batch, rows, h_q, d], q_dtype NBX_F32 or NBX_BF16
  *   k_pool, v_pool [device] [num_pages, h_kv, page_tokens, d] in pool_dtype
