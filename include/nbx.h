@@ -71,7 +71,8 @@ typedef enum {
 /* Positions per staged tile: every page must hold a whole number of tiles, so no
  * tile straddles two pages (paged_decode_attention's "ZERO FALLBACK" check). */
 #define NBX_TILE_POSITIONS 16
-/* The split rule (nbxtensor/ops/paged_decode_attn.py, paged_decode_splits). */
+/* The pages' split rule (nbxtensor/ops/paged_decode_attn.py, paged_decode_splits): it bounds the
+ * splits a workspace holds; the decode itself cuts splits of two of these (see nbx_paged_decode_attn). */
 #define NBX_SPLIT_POSITIONS 256
 #define NBX_MAX_SPLITS 64
 
@@ -127,9 +128,9 @@ NBX_API size_t nbx_paged_decode_workspace_bytes_for(int q_dtype, int pool_dtype,
  * p = seq_lens[b] - rows + r and attends keys 0..p of KV head h / (h_q / h_kv):
  *   s_j = scale * k_scale * (q . k_j),  out = v_scale * sum_j e^(s_j - max s) v_j / sum_j e^(s_j - max s).
  * A row with no visible key (p < 0, or seq_lens[b] == 0) gets 0. Each sequence is cut into
- * min(ceil(len/256), 64) splits of whole pages (a window on tensor cores, see
- * nbx_paged_decode_partial_kernel: about one work unit per SM in all, splits in proportion to the
- * lengths, at most as many as the pages' rule gives at max_seq_len); each split's unnormalised
+ * min(ceil(len/512), 64) splits of whole pages, two of the pages' 256-position splits each (a window
+ * on tensor cores, see nbx_paged_decode_partial_kernel: about one work unit per SM in all, splits in
+ * proportion to the lengths, at most min(ceil(max_seq_len/256), 64)); each split's unnormalised
  * partial (m, l, acc) is computed with an fp32 online softmax and the partials are merged in
  * ascending split order (a split with m = -inf is skipped, so NaN inputs reach the output). The
  * result does not depend on the physical page ids or on the order the work runs in.

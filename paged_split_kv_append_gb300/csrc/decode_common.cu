@@ -9,6 +9,12 @@ namespace nbx {
 constexpr int kPlanThreads = 256;
 constexpr int kSortMax = 2048;   // batches up to this size are planned in shared memory, longest split first
 
+// Positions per split of the SIMT partial kernel: two of the pages' splits (NBX_SPLIT_POSITIONS).
+// Each work unit of the persistent kernel pays about 2.4 us at its boundaries (the cross-warp merge
+// and the partial's stores, the next unit's query staging and first stage); at 512 positions a unit
+// single_row's decode call took 109.4 against 115.5 us at 256 (ragged 754.1 against 755.9 us).
+constexpr int kSimtSplitPositions = 2 * NBX_SPLIT_POSITIONS;
+
 int splits_for(int length) {
   const int l = length < 1 ? 1 : length;
   int s = (l + NBX_SPLIT_POSITIONS - 1) / NBX_SPLIT_POSITIONS;
@@ -125,7 +131,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
       const int cap_s = min(p.max_splits, max(1, L / 64));
       S = static_cast<int>(want < 1 ? 1 : (want > cap_s ? cap_s : want));
     } else {
-      S = (max(L, 1) + NBX_SPLIT_POSITIONS - 1) / NBX_SPLIT_POSITIONS;
+      // two of the pages' 256-position splits a split: half the unit boundaries, at most 64 splits
+      S = (max(L, 1) + kSimtSplitPositions - 1) / kSimtSplitPositions;
       S = S > NBX_MAX_SPLITS ? NBX_MAX_SPLITS : S;
     }
     int seg = (L + S - 1) / S;

@@ -3,8 +3,8 @@
 //
 // Method (nbxtensor/ops/paged_decode_attn.py, paged_decode_splits and
 // paged_decode_attn_split_kernel; nbxtensor/ops/attention_wrappers.py, decode_reduce):
-// every sequence is cut into min(ceil(len/256), 64) splits of whole pages (the plan kernel sizes a
-// tensor-core window's splits differently: about one work unit per SM); each split runs an
+// every sequence is cut into splits of whole pages (the pages' 256 positions; here two of those a
+// split, and a tensor-core window's sized for about one work unit per SM); each split runs an
 // online softmax over its keys and stores an unnormalised partial (m, l, acc); the partials of
 // a query row are merged in ascending split order.
 //

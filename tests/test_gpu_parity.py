@@ -176,10 +176,11 @@ def test_nan_key_reaches_the_output():
 
 
 def test_split_of_only_nan_keys_reaches_the_output():
-    # every key of the second split is NaN: its running max is NaN, and the merge keeps it
-    case = wl.make_case("single_row_small", device=DEV, lens=[300, 40])
+    # every key of the second split is NaN (600 positions: two splits of 304 and 296 positions): its
+    # running max is NaN, and the merge keeps it
+    case = wl.make_case("single_row_small", device=DEV, lens=[600, 40])
     lo = int(case.tok_offset[0])
-    case.k_raw[lo + 160:lo + 300, 1, :] = float("nan")
+    case.k_raw[lo + 304:lo + 600, 1, :] = float("nan")
     sess, out = run_step(case)
     o = out.cpu().numpy()
     G = case.cfg.group

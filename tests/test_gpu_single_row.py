@@ -1,6 +1,6 @@
 """GPU parity of plain decode (one query row, bf16 q and pools, d 128: the single-row configs) against
 the float64 oracle, across GQA groups, page sizes and lengths around the kernel's 16-position tiles,
-32-position stages and 256-position splits.
+32-position stages and 512-position splits.
 
 Same bars as the other decode tests: max |err| 2e-3 against the oracle, bit-identical under grid size
 and page placement, pools starting as NaN so that any read past a sequence shows up.
@@ -47,9 +47,9 @@ def test_head_layouts_and_page_sizes(h_q, h_kv, page):
         assert torch.equal(o2, out), f"grid limit {limit}"
 
 
-# lengths at and around the 16-position tile, the 32-position stage, the 256-position split and
+# lengths at and around the 16-position tile, the 32-position stage, the 512-position split and
 # longer splits; 0 (no unit, zero output)
-EDGE = (0, 1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 383, 384, 385, 511, 512, 513, 4097)
+EDGE = (0, 1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 511, 512, 513, 767, 768, 769, 1023, 1024, 1025, 4097)
 
 
 def test_edge_lengths_across_tiles():
