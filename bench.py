@@ -49,16 +49,15 @@ KERNEL_SOURCES = ("paged_split_kv_append_gb300/csrc/decode_kernels.cuh",
 
 
 # ------------------------------------------------------------------------------------------ shared set-up
-def session_for_case(case: "wl.Case", device, fill_nan: bool = True, prefill: bool = True, widen: bool = True):
+def session_for_case(case: "wl.Case", device, fill_nan: bool = True, prefill: bool = True):
     """The device state of one workload: pools prefilled through nbx_paged_kv_append with every
-    position but the step's, and the step's inputs (queries, tables, lengths, new tokens).
-    widen=False sizes the workspace without room for the bf16 copies of an fp8 pool."""
+    position but the step's, and the step's inputs (queries, tables, lengths, new tokens)."""
     from paged_split_kv_append_gb300.session import PagedDecodeSession
     cfg = case.cfg
     sess = PagedDecodeSession(num_pages=case.num_pages, h_kv=cfg.h_kv, page_tokens=cfg.page_tokens, d=cfg.d,
                               pool_dtype=cfg.pool_dtype, batch=cfg.batch, rows=cfg.rows, h_q=cfg.h_q,
                               max_seq_len=case.max_seq_len, device=device, fill_nan=fill_nan,
-                              q_dtype=cfg.q_dtype, widen=widen)
+                              q_dtype=cfg.q_dtype)
     sess.k_scale, sess.v_scale = case.k_scale, case.v_scale
     if prefill:
         idx, slots = case.prefill_index()
@@ -440,10 +439,9 @@ def time_case(case, dev, steps: int, warmup: int, flush, sink, stream, e2e_steps
         raise RuntimeError(f"device status {sess.status_bits():#x} after the timed steps")
     step_ms = [a.elapsed_time(b) for a, b in ev]
     dec_ms = [a.elapsed_time(b) for a, b in kev]
-    # our kernels per call: append (when the step has new tokens), plan, partial, the merge when some
-    # sequence can have more than one split, and the widen kernel of an fp8 window on tensor cores
-    widen = 1 if partial_kernel_name(case.cfg).startswith("widen") else 0
-    decode_launches = 2 + (1 if case.max_seq_len > 256 else 0) + widen
+    # our kernels per call: append (when the step has new tokens), plan, partial, and the merge when
+    # some sequence can have more than one split
+    decode_launches = 2 + (1 if case.max_seq_len > 256 else 0)
     step_launches = decode_launches + (1 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 0)
     r = dict(step_ms=step_ms, ms_per_step=sum(step_ms) / len(step_ms), dec_ms=sum(dec_ms) / len(dec_ms),
              launches=(step_launches + decode_launches) * steps, partial=partial_kernel_name(case.cfg))
@@ -552,9 +550,7 @@ def partial_kernel_name(cfg) -> str:
     code = {"f32": nbx.NBX_F32, "bf16": nbx.NBX_BF16, "e4m3": nbx.NBX_E4M3}
     kind = nbx.nbx_paged_decode_partial_kernel(code[cfg.q_dtype], code[cfg.pool_dtype], cfg.rows, cfg.h_q, cfg.h_kv,
                                                cfg.d, 1, cfg.page_tokens)
-    if kind == nbx.PARTIAL_TCGEN05_WIDENED:
-        return "widen_kernel + decode_partial_mma_kernel"
-    return "decode_partial_mma_kernel" if kind == nbx.PARTIAL_TCGEN05 else "decode_partial_kernel"
+    return "decode_partial_kernel" if kind == nbx.PARTIAL_SIMT else "decode_partial_mma_kernel"
 
 
 def barrier(world: int):

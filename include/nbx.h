@@ -109,12 +109,10 @@ NBX_API int nbx_paged_kv_append(const void* new_k, const void* new_v, int new_dt
 NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len);
 
 /*
- * nbx_paged_decode_workspace_bytes_for -- the workspace for these sizes and formats, with room for
- * the bf16 copies an fp8 (NBX_E4M3) pool needs to run on tensor cores when the call qualifies
- * (nbx_paged_decode_partial_kernel returns NBX_PARTIAL_TCGEN05_WIDENED): 2 x batch x
- * ceil(max_seq_len / 64) x 64 x h_kv x d x 2 bytes more. This library addition has no counterpart in
- * the method's pages. For every other case it equals nbx_paged_decode_workspace_bytes. Returns 0
- * if the sizes are invalid.
+ * nbx_paged_decode_workspace_bytes_for -- the workspace for these sizes and formats. Every format
+ * and page size needs the same today (the tensor-core kernel reads an fp8 pool's codes as they are
+ * stored), so it equals nbx_paged_decode_workspace_bytes; the formats are taken so that a caller
+ * sizing per call keeps working if that changes. Returns 0 if the sizes are invalid.
  */
 NBX_API size_t nbx_paged_decode_workspace_bytes_for(int q_dtype, int pool_dtype, int batch, int rows, int h_q,
                                                     int h_kv, int d, int max_seq_len, int page_tokens);
@@ -144,9 +142,7 @@ NBX_API size_t nbx_paged_decode_workspace_bytes_for(int q_dtype, int pool_dtype,
  *   scale        softmax scale (finite); k_scale, v_scale: pool scales (finite, > 0)
  *   out          [device] fp32 [batch, rows, h_q, d]
  *   workspace    [device] at least nbx_paged_decode_workspace_bytes(...) bytes, 256-byte aligned;
- *                its contents need no initialisation and are overwritten. With an fp8 pool and a
- *                workspace of nbx_paged_decode_workspace_bytes_for(...) bytes, a multi-row window runs
- *                on tensor cores over exact bf16 copies of its K/V made in the workspace
+ *                its contents need no initialisation and are overwritten
  *   status       [device] int32 or NULL
  *   stream       cudaStream_t
  * Requirements: h_q % h_kv == 0; d in {64, 128, 256}; page_tokens a multiple of
@@ -250,7 +246,7 @@ NBX_API int nbx_paged_decode_bounds(const void* q, int q_dtype, int batch, int r
  * floor((C(n) + 125) / 2): a row with U <= gate and max |v| <= 256 takes its weights as 2^(z - m),
  * m = ceil(U) - C(n), fixed before the split is read (no running max, no rescale; no weight above 2^C
  * or below 2^-125). A row that fails the gate, and every row of a window whose P enters the product
- * in f16 (an fp8 pool widened on tensor cores: f16 cannot hold 2^C), keeps the online max. Calls that
+ * as E4M3 terms (an fp8 pool on tensor cores: E4M3 cannot hold 2^C), keeps the online max. Calls that
  * run the SIMT kernel are the same as nbx_paged_decode_attn. Results are within the decode's tolerance
  * of nbx_paged_decode_attn's.
  *
@@ -301,9 +297,8 @@ NBX_API int nbx_paged_decode_attn_noalloc(const void* q, int q_dtype, int batch,
 typedef enum {
     NBX_PARTIAL_SIMT = 0,            /* CUDA cores: work units of 4 query vectors, any supported shape */
     NBX_PARTIAL_TCGEN05 = 1,         /* tensor cores (tcgen05.mma): work units of 128 query vectors */
-    NBX_PARTIAL_TCGEN05_WIDENED = 2  /* fp8 pool: the tensor-core kernel on bf16 copies of the sequences'
-                                        K/V in the workspace, when the call's workspace holds them
-                                        (nbx_paged_decode_workspace_bytes_for); otherwise SIMT */
+    NBX_PARTIAL_TCGEN05_FP8 = 2      /* fp8 (E4M3) pool: the tensor-core kernel on the codes as stored
+                                        (tcgen05.mma kind::f8f6f4), Q and P as two E4M3 terms each */
 } nbx_partial_kernel;
 
 /*
@@ -315,10 +310,10 @@ typedef enum {
  * Returns NBX_PARTIAL_TCGEN05 when rows * (h_q / h_kv) >= 64, h_q / h_kv <= 128, q_dtype and
  * pool_dtype are both NBX_BF16, d is 128 or 256, page_tokens is a multiple of 64 and the pool has
  * fewer than 2^31 - 64 rows of d elements per K or V (the call itself also needs scale > 0; a
- * decode with scale <= 0 runs the SIMT kernel); NBX_PARTIAL_SIMT for every other supported case; a negative
- * nbx_status for arguments nbx_paged_decode_attn rejects (shape, page alignment, dtype). Both
- * kernels compute the same partials to within the decode's tolerance; neither depends on page
- * ids or on the grid size.
+ * decode with scale <= 0 runs the SIMT kernel); NBX_PARTIAL_TCGEN05_FP8 under the same conditions
+ * with an NBX_E4M3 pool; NBX_PARTIAL_SIMT for every other supported case; a negative nbx_status for
+ * arguments nbx_paged_decode_attn rejects (shape, page alignment, dtype). The kernels compute the
+ * same partials to within the decode's tolerance; none depends on page ids or on the grid size.
  */
 NBX_API int nbx_paged_decode_partial_kernel(int q_dtype, int pool_dtype, int rows, int h_q, int h_kv, int d,
                                             int num_pages, int page_tokens);

@@ -31,7 +31,7 @@ __all__ = [
 
 NBX_F32, NBX_BF16, NBX_E4M3 = 0, 1, 2
 DEV_BAD_SLOT, DEV_BAD_PAGE, DEV_BAD_LEN, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
-PARTIAL_SIMT, PARTIAL_TCGEN05, PARTIAL_TCGEN05_WIDENED = 0, 1, 2
+PARTIAL_SIMT, PARTIAL_TCGEN05, PARTIAL_TCGEN05_FP8 = 0, 1, 2
 
 _lib = None
 _lock = threading.Lock()

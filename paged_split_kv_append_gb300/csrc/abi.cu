@@ -129,8 +129,8 @@ NBX_API int nbx_paged_decode_partial_kernel(int q_dtype, int pool_dtype, int row
   p.num_pages = num_pages;
   p.page_tokens = page_tokens;
   p.qk_scale_log2 = 1.f;   // a positive softmax scale
-  if (widen_path_applies(q_dtype, pool_dtype, rows, h_q, h_kv, d, page_tokens)) return NBX_PARTIAL_TCGEN05_WIDENED;
-  return mma_path_applies(p, q_dtype, pool_dtype) ? NBX_PARTIAL_TCGEN05 : NBX_PARTIAL_SIMT;
+  if (!mma_path_applies(p, q_dtype, pool_dtype)) return NBX_PARTIAL_SIMT;
+  return pool_dtype == NBX_E4M3 ? NBX_PARTIAL_TCGEN05_FP8 : NBX_PARTIAL_TCGEN05;
 }
 
 NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len) {
@@ -143,11 +143,11 @@ NBX_API size_t nbx_paged_decode_workspace_bytes(int batch, int rows, int h_q, in
 NBX_API size_t nbx_paged_decode_workspace_bytes_for(int q_dtype, int pool_dtype, int batch, int rows, int h_q,
                                                     int h_kv, int d, int max_seq_len, int page_tokens) {
   if (!decode_shape_ok(batch, rows, h_q, h_kv, d, max_seq_len)) return 0;
+  (void)q_dtype;
+  (void)pool_dtype;
+  (void)page_tokens;
   WorkspaceLayout w;
-  const bool widen = page_tokens > 0 && widen_path_applies(q_dtype, pool_dtype, rows, h_q, h_kv, d, page_tokens);
-  if (!workspace_layout(batch, rows, h_q, h_kv, d, max_seq_len, &w, widen)) {
-    if (!workspace_layout(batch, rows, h_q, h_kv, d, max_seq_len, &w)) return 0;
-  }
+  if (!workspace_layout(batch, rows, h_q, h_kv, d, max_seq_len, &w)) return 0;
   return w.total;
 }
 
@@ -176,11 +176,6 @@ static int decode_call(const void* q, int q_dtype, int batch, int rows, int h_q,
   WorkspaceLayout w;
   if (!workspace_layout(batch, rows, h_q, h_kv, d, max_seq_len, &w)) return NBX_ERR_SHAPE;
   if (workspace_bytes < w.total) return NBX_ERR_WORKSPACE;
-  // fp8 pool with a multi-row window: the tensor-core kernel on bf16 copies when the workspace holds them
-  WorkspaceLayout ww;
-  const bool widen = scale > 0.f && widen_path_applies(q_dtype, pool_dtype, rows, h_q, h_kv, d, page_tokens) &&
-                     workspace_layout(batch, rows, h_q, h_kv, d, max_seq_len, &ww, true) && workspace_bytes >= ww.total;
-  if (widen) w = ww;
 
   char* ws = static_cast<char*>(workspace);
   DecodeParams p = {};
@@ -214,10 +209,6 @@ static int decode_call(const void* q, int q_dtype, int batch, int rows, int h_q,
   p.row_blocks = w.row_blocks;
   p.qk_scale_log2 = scale * k_scale * kLog2eHost;
   p.v_scale = v_scale;
-  p.widen_k = widen ? ws + w.widen_k : nullptr;
-  p.widen_v = widen ? ws + w.widen_v : nullptr;
-  p.widen_bt = widen ? reinterpret_cast<int32_t*>(ws + w.widen_bt) : nullptr;
-  p.t64 = w.t64;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.fs_q_norm = fs_q_norm;
   p.fs_kv_max = fs_kv_max;

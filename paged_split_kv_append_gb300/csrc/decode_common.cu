@@ -21,8 +21,7 @@ int splits_for(int length) {
   return s < 1 ? 1 : (s > NBX_MAX_SPLITS ? NBX_MAX_SPLITS : s);
 }
 
-bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* w,
-                      bool widen) {
+bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* w) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t S = static_cast<size_t>(splits_for(max_seq_len));
   const size_t rb = (static_cast<size_t>(rows) * (h_q / h_kv) + kQB - 1) / kQB;
@@ -43,20 +42,6 @@ bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq
   off += up(prow * 4);
   w->acc_part = off;
   off += up(prow * static_cast<size_t>(d) * 4);
-  w->t64 = 0;
-  w->widen_k = w->widen_v = w->widen_bt = off;
-  if (widen) {
-    const size_t t64 = (static_cast<size_t>(max_seq_len < 1 ? 1 : max_seq_len) + 63) / 64;
-    const size_t bytes = static_cast<size_t>(batch) * t64 * h_kv * 64 * d * 2;
-    if (static_cast<size_t>(batch) * t64 * h_kv * 64 >= (static_cast<size_t>(1) << 31) - 64) return false;
-    w->t64 = static_cast<int>(t64);
-    w->widen_k = off;
-    off += up(bytes);
-    w->widen_v = off;
-    off += up(bytes);
-    w->widen_bt = off;
-    off += up(static_cast<size_t>(batch) * t64 * 4);
-  }
   w->total = off;
   w->max_splits = static_cast<int>(S);
   w->row_blocks = static_cast<int>(rb);
@@ -522,8 +507,9 @@ cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit,
                             cudaStream_t stream) {
   DecodeParams q = p;
-  q.part_f16 = p.widen_k != nullptr ? 1 : 0;   // fp8 windows on tensor cores: f16 partials
-  if (p.widen_k != nullptr || mma_path_applies(p, q_dtype, pool_dtype)) {
+  const bool mma = mma_path_applies(p, q_dtype, pool_dtype);
+  q.part_f16 = mma && pool_dtype == NBX_E4M3 ? 1 : 0;   // fp8 pools on tensor cores: f16 partials
+  if (mma) {
     // a tensor-core window: splits sized for one wave of work units over the GPU's SMs (the grid
     // limit does not enter, so the partition, and the result, is the same at any grid size)
     q.tc_units = device_info().sm_count;
@@ -532,8 +518,7 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
   cudaError_t e = q.tc_units > 0 ? launch_pdl(plan_kernel<true>, 1u, kPlanThreads, 0, stream, q)
                                  : launch_pdl(plan_kernel<false>, 1u, kPlanThreads, 0, stream, q);
   if (e != cudaSuccess) return e;
-  if (q.widen_k != nullptr) e = decode_dispatch_widened(q, grid_limit, stream);
-  else if (mma_path_applies(q, q_dtype, pool_dtype)) e = decode_dispatch_mma(q, grid_limit, stream);
+  if (mma) e = decode_dispatch_mma(q, pool_dtype, grid_limit, stream);
   else if (pool_dtype == NBX_F32) e = decode_dispatch_F32(q, q_dtype, grid_limit, stream);
   else if (pool_dtype == NBX_BF16) e = decode_dispatch_BF16(q, q_dtype, grid_limit, stream);
   else e = decode_dispatch_E4M3(q, q_dtype, grid_limit, stream);

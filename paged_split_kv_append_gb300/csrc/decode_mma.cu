@@ -12,9 +12,10 @@
 //  * Work unit = (split entry, KV head, M tile), M tile fastest. The query vectors of one KV head,
 //    v = row * G + head, are cut into M tiles of 128 (a tile may split one row's heads), so no tile
 //    row is padding but in the last tile. Static round-robin over the plan's longest-first list.
-//  * Shared memory: the unit's Q tile (128-byte-swizzled K-major atoms of 64 columns), a K ring and
-//    a V ring of 16 KB slots (64 positions x 128 columns: half of a d=256 tile, a whole d=128
-//    tile; a tile is one page or a 64-aligned part of one). Every slot has a full barrier (TMA bytes) and an empty barrier (its consumer).
+//  * Shared memory: the unit's Q tile (128-byte-swizzled K-major atoms of 128 bytes a row), a K ring
+//    and a V ring of 16 KB slots (64 positions x 128 bf16 columns: half of a d=256 tile, a whole
+//    d=128 tile; or 64 positions x d E4M3 codes, a whole tile; a tile is one page or a 64-aligned
+//    part of one). Every slot has a full barrier (TMA bytes) and an empty barrier (its consumer).
 //  * warps 4 and 6 (producers) fill the K ring and the V ring with TMA (cp.async.bulk.tensor),
 //    one thread issuing while the warp's lanes fetch block-table ids a chunk ahead. A page id
 //    outside the pool loads rows before the tensor, which read as zeros; its positions are
@@ -22,21 +23,34 @@
 //  * TMEM (512 columns): three S/P buffers [0, 192), O [192, 192 + d). Three buffers let QK^T run
 //    two tiles ahead of PV.
 //  * Two issuing threads share the tensor pipe, each a plain sequence of bounded waits and MMAs
-//    (kind::f16, bf16 x bf16 -> fp32 in TMEM, completions signalled with tcgen05.commit):
-//      warp 5:  S[x % 3] = Q K(x)^T   M=128, N=64, K=d; Q and K from shared memory; its lanes 1-31
-//               copy each unit's Q tile (16-byte cp.async into the swizzled atoms, zeros past the
-//               last vector) once the previous unit's last QK^T has completed
-//      warp 7:  O += P_hi(y) V(y) + P_lo(y) V(y)   M=128, N=d (both V halves in one MMA), K=64;
+//    (fp32 accumulators in TMEM, completions signalled with tcgen05.commit):
+//      warp 5:  S[x % 3] = Q K(x)^T   M=128, N=64, K=d; Q and K from shared memory; with a bf16
+//               pool (kind::f16) its lanes 1-31 copy each unit's Q tile (a tensor box, or 16-byte
+//               cp.async into the swizzled atoms, zeros past the last vector) once the previous
+//               unit's last QK^T has completed
+//      warp 7:  O += P_hi(y) V(y) + P_lo(y) V(y)   M=128, N=d (all V columns in one MMA), K=64;
 //               P from TMEM. It zeroes V rows past a split's end before their PV (0 x NaN would
-//               otherwise leak) and skips 16-position steps that hold none.
+//               otherwise leak) and skips K steps that hold none.
 //    Split between two threads, the per-tile control work of one overlaps the other's MMAs. With
 //    a bf16 pool P enters the product as two bf16 terms, P_hi = p truncated to bf16 and
-//    P_lo = (p - P_hi) truncated, so the weights keep 15 bits or more. With the exact copies of an
-//    fp8 pool V is f16 and P enters as one f16 term rounded to nearest (11 bits), halving PV.
+//    P_lo = (p - P_hi) truncated, so the weights keep 15 bits or more.
+//  * An fp8 (E4M3) pool is read as it is stored: kind::f8f6f4 MMAs on the codes, K=32 a step. Q
+//    enters as two E4M3 terms, Q_hi + Q_lo, of the query vector times a power of two 2^e that puts
+//    its largest element in [128, 256): Q_hi holds 4 significant bits (rounded to nearest by a
+//    Veltkamp split), Q_lo the rest, so a bf16 element of at least 2^-9 of the vector's largest
+//    is exact and the others are off by at most 2^-16 of it; the softmax threads write them (one
+//    query vector each) and fold 2^-e into their row's scale. P enters as P_hi + P_lo, the same
+//    split of p: each p is off by at most 2^-9 p, plus 2^-9 when p < 2^-1 (E4M3 holds nothing
+//    below 2^-9). The running max m moves up when a tile's max passes m + 8.75 (p stays below
+//    448) and down when a tile holds more weights below 2^-1 than its largest weight, so each
+//    tile's weights are off by at most 2^-8 of their sum.
+//    O and l are rescaled in TMEM whenever m moves, downwards only while the weight gathered stays
+//    below 2^40 (past that the tile, below 2^15, adds less than 2^-25 of the total).
 //  * warps 0-3 (softmax, one query vector per thread = one TMEM lane): read S from TMEM, mask
 //    (split end, causal row position, missing pages), run the online softmax in log2 units with
-//    the lazy rescale (O is rescaled in TMEM only when a row's max grows by more than 2^8), and
-//    write P_hi / P_lo over the S columns they came from. After the unit's last PV each thread
+//    the lazy rescale (O is rescaled in TMEM only when a row's max grows by more than 2^8; with an
+//    fp8 pool, also when it falls, as above), and write P_hi / P_lo over the S columns they came
+//    from. After the unit's last PV each thread
 //    stores its own row of O, 32 columns at a time, from registers with 32-byte stores -- the
 //    partial, or the normalised output when the sequence has one split.
 //  * Every wait is bounded. On timeout the kernel records NBX_DEV_TIMEOUT, waits (bounded) for
@@ -61,14 +75,19 @@ constexpr int kSoftmaxThreads = 128;
 constexpr float kMmaTau = 8.0f;  // lazy-rescale threshold, log2 units
 constexpr int kChunk = 32;       // output columns per epilogue step
 constexpr int kSBufs = 3;        // S/P buffers in TMEM
-constexpr int kSlotBytes = 16384;  // ring slot: 64 positions x 128 columns bf16
+constexpr int kSlotBytes = 16384;  // ring slot: 64 positions x 128 columns bf16, or x d E4M3 codes
+constexpr int kAtomBytes = kMmaN * 128;   // one 128-byte-wide swizzle column of a 64-position tile
+// fp8 pools: the running max sits kF8Mid below a tile's max after a move; it moves up when a
+// tile's max passes m + kF8Hi (p <= 2^8.75 = 430, below 448, the largest E4M3), down only while
+// the gathered weight stays <= 2^40
+constexpr float kF8Hi = 8.75f, kF8Mid = 6.f, kF8MaxWeight = 1099511627776.f;
 
-template <int D>
+template <int D, bool F8>
 struct MmaCfg {
-  static constexpr int kHalves = D / 128;                  // ring slots per K (or V) tile
+  static constexpr int kHalves = F8 ? 1 : D / 128;         // ring slots per K (or V) tile
   static constexpr int kKSlots = D <= 128 ? 5 : 4;         // K ring
   static constexpr int kVSlots = kKSlots;                  // V ring
-  static constexpr int kQBytes = kMmaM * D * 2;            // Q tile, D / 64 atoms of 16 KB
+  static constexpr int kQBytes = kMmaM * D * 2;            // Q tile (bf16, or E4M3 Q_hi and Q_lo): atoms of 16 KB
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + kKSlots * kSlotBytes;
@@ -229,12 +248,97 @@ struct PageStream {
   __device__ __forceinline__ int page(int t) const { return __shfl_sync(0xffffffffu, cur, t & 31); }
 };
 
-// PvF16: V is f16 (the exact f16 copies of an fp8 pool) and P enters PV as one f16 term, rounded
-// to nearest; otherwise V is bf16 and P enters as P_hi + P_lo.
-template <int D, bool PvF16>
+// Two floats to two E4M3 codes, rounded to nearest (saturating; NaN stays NaN), a in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_rn(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+// x = hi + lo exactly, hi = x rounded to nearest with 4 significant bits (Veltkamp's splitting with
+// the factor 2^20 + 1 on 24-bit significands; no operation may be fused or reordered, hence the _rn
+// intrinsics). x of an E4M3 term: |x| <= 2^8, far from overflow.
+__device__ __forceinline__ void split4(float x, float& hi, float& lo) {
+  const float c = __fmul_rn(x, 1048577.0f);
+  hi = __fsub_rn(c, __fsub_rn(c, x));
+  lo = __fsub_rn(x, hi);
+}
+
+// Four weights (positions 4i .. 4i + 3 of a tile) as the E4M3 terms P_hi and P_lo, four codes a word.
+__device__ __forceinline__ void p_terms4(const float* pv, uint32_t& wh, uint32_t& wl) {
+  float h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) split4(pv[q], h[q], l[q]);
+  wh = e4m3x2_rn(h[0], h[1]) | (e4m3x2_rn(h[2], h[3]) << 16);
+  wl = e4m3x2_rn(l[0], l[1]) | (e4m3x2_rn(l[2], l[3]) << 16);
+}
+
+// fp8 pools: this thread's query vector of unit `mu` as the terms Q_hi and Q_lo (E4M3) of the
+// vector times 2^e, its largest |element| brought into [128, 256), written into row `row` of the
+// Q tile's 128-byte-swizzled K-major atoms: Q_hi atoms first, then Q_lo. Rows past the last vector
+// are zero; a vector holding NaN or infinity gets NaN codes. Returns 2^-e, which the row's scores
+// take back.
+template <int D>
+__device__ __forceinline__ float q_to_e4m3_terms(const DecodeParams& p, const MmaUnit& mu, int row, char* q_s) {
+  const int G = p.group;
+  const int vq = mu.mt * kMmaM + row;
+  const bool ok = vq < p.rows * G;
+  const int r = ok ? vq / G : 0, gq = ok ? vq - r * G : 0;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      static_cast<const char*>(p.q) +
+      (((static_cast<int64_t>(mu.b) * p.rows + r) * p.h_q) + static_cast<int64_t>(mu.h) * G + gq) * (D * 2));
+  float amax = 0.f;
+  if (ok) {
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 v = __ldg(src + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = bf16x2_to_float2(w[i]);
+        amax = max_nan(amax, max_nan(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+  }
+  const bool bad = !(amax <= 3.402823466e38f);   // NaN or infinity in the vector
+  int e = 0;
+  if (!bad && amax > 0.f) {
+    const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;   // floor(log2 amax), normal amax
+    e = min(120, max(-120, 7 - ex));
+  }
+  const float sc = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);   // 2^e
+  char* row_hi = q_s + row * 128;
+  char* row_lo = q_s + (D / 128) * (kMmaM * 128) + row * 128;
+#pragma unroll 2
+  for (int c = 0; c < D / 16; ++c) {   // 16 elements: one 16-byte chunk of each term
+    uint4 ph = make_uint4(0u, 0u, 0u, 0u), pl = ph;
+    if (ok) {
+      const uint4 v0 = __ldg(src + 2 * c), v1 = __ldg(src + 2 * c + 1);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = bf16x2_to_float2(w[2 * i]), b = bf16x2_to_float2(w[2 * i + 1]);
+        const float x[4] = {__fmul_rn(a.x, sc), __fmul_rn(a.y, sc), __fmul_rn(b.x, sc), __fmul_rn(b.y, sc)};
+        p_terms4(x, hw[i], lw[i]);
+      }
+      ph = bad ? make_uint4(0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu, 0x7f7f7f7fu) : make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      pl = bad ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    const int a = c >> 3, cc = c & 7;   // 128-byte atom and its 16-byte chunk
+    const int off = a * (kMmaM * 128) + ((cc ^ (row & 7)) << 4);
+    *reinterpret_cast<uint4*>(row_hi + off) = ph;
+    *reinterpret_cast<uint4*>(row_lo + off) = pl;
+  }
+  return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
+// F8: the pools hold E4M3 codes, read as they are by kind::f8f6f4 MMAs (Q and P as two E4M3 terms
+// each); otherwise bf16 pools and kind::f16 MMAs (P as two bf16 terms).
+template <int D, bool F8>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     decode_partial_mma_kernel(DecodeParams p, const __grid_constant__ MmaMaps maps) {
-  using C = MmaCfg<D>;
+  using C = MmaCfg<D, F8>;
   constexpr int NK = C::kKSlots;
   constexpr int NV = C::kVSlots;
   constexpr int HI = C::kHalves;
@@ -284,8 +388,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       mbar_init(&p_full[i], kSoftmaxThreads);
       mbar_init(&sp_free[i], 1);
     }
-    // a tensor box (one arrival with the byte count) or the cp.async completions of lanes 1-31
-    mbar_init(q_full, whole_row_tile_rows(p.rows, p.group) > 0 ? 1 : 31);
+    // the E4M3 terms of the 128 softmax threads, a tensor box (one arrival with the byte count), or
+    // the cp.async completions of lanes 1-31
+    mbar_init(q_full, F8 ? kSoftmaxThreads : (whole_row_tile_rows(p.rows, p.group) > 0 ? 1 : 31));
     mbar_init(q_empty, 1);
     mbar_init(o_free, kSoftmaxThreads);
     mbar_init(done_bar, 1);
@@ -337,9 +442,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
         if (lane == 0) {
           char* dst = rbase + (i % NR) * kSlotBytes;
-          mbar_arrive_expect_tx(&rfull[i % NR], kSlotBytes);
-          tma_load_2d(dst, map, (2 * j) * 64, row0, &rfull[i % NR]);
-          tma_load_2d(dst + kMmaN * 128, map, (2 * j + 1) * 64, row0, &rfull[i % NR]);
+          if constexpr (F8) {   // the tile's D codes a position, 128 a box
+            mbar_arrive_expect_tx(&rfull[i % NR], kMmaN * D);
+#pragma unroll
+            for (int a = 0; a < D / 128; ++a) tma_load_2d(dst + a * kAtomBytes, map, a * 128, row0, &rfull[i % NR]);
+          } else {              // 128 bf16 columns of the tile, 64 a box
+            mbar_arrive_expect_tx(&rfull[i % NR], kSlotBytes);
+            tma_load_2d(dst, map, (2 * j) * 64, row0, &rfull[i % NR]);
+            tma_load_2d(dst + kAtomBytes, map, (2 * j + 1) * 64, row0, &rfull[i % NR]);
+          }
         }
       }
       if (!ok) break;
@@ -362,7 +473,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     TileIter it;
     it.begin(p, m_tiles, n_units, HI);
     if (lane == 0) {
-      constexpr uint32_t kIdescS = mma_idesc(kMmaM, kMmaN, false);
+      constexpr uint32_t kIdescS = mma_idesc(kMmaM, kMmaN, false, F8);   // bf16, or E4M3 (format 0)
       bool ok = true;
       uint32_t sx = 0, sxp = 0;   // S/P buffer (x % 3) and its phase count (x / 3)
       while (!it.done) {
@@ -373,14 +484,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (ok && it.t == 0) ok = bwait(q_full, it.k & 1u, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        if (it.t == 0) fence_proxy_async();   // Q was written by cp.async (generic proxy)
+        if (it.t == 0) fence_proxy_async();   // Q was written by cp.async or st.shared (generic proxy)
+        if constexpr (F8) {
+          // S = Q_hi K^T + Q_lo K^T, 32 codes of d a step: 128-byte atoms of Q and of the K slot
+          const uint32_t kb = smem_u32(kring + (ki % NK) * kSlotBytes);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t a = kk >> 2, sub = kk & 3;   // 64-column atom, 16-column step in it
-          const uint64_t ad = smem_desc(q_addr + a * (kMmaM * 128) + sub * 32, 16, 1024);
-          const uint32_t kb = smem_u32(kring + ((ki + (a >> 1)) % NK) * kSlotBytes) + (a & 1) * (kMmaN * 128);
-          const uint64_t bd = smem_desc(kb + sub * 32, 16, 1024);
-          tc_mma_ss(tmem + sx * kMmaN, ad, bd, kIdescS, kk > 0);
+          for (int term = 0; term < 2; ++term)
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              const uint32_t a = kk >> 2, sub = kk & 3;
+              const uint64_t ad = smem_desc(q_addr + (term * (D / 128) + a) * (kMmaM * 128) + sub * 32, 16, 1024);
+              const uint64_t bd = smem_desc(kb + a * kAtomBytes + sub * 32, 16, 1024);
+              tc_mma_ss_f8(tmem + sx * kMmaN, ad, bd, kIdescS, term > 0 || kk > 0);
+            }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t a = kk >> 2, sub = kk & 3;   // 64-column atom, 16-column step in it
+            const uint64_t ad = smem_desc(q_addr + a * (kMmaM * 128) + sub * 32, 16, 1024);
+            const uint32_t kb = smem_u32(kring + ((ki + (a >> 1)) % NK) * kSlotBytes) + (a & 1) * kAtomBytes;
+            const uint64_t bd = smem_desc(kb + sub * 32, 16, 1024);
+            tc_mma_ss(tmem + sx * kMmaN, ad, bd, kIdescS, kk > 0);
+          }
         }
         tc_commit(&s_full[sx]);
         for (int j = 0; j < HI; ++j) tc_commit(&kempty[(ki + j) % NK]);
@@ -398,7 +523,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // every QK^T of this CTA has completed before the TMEM is released
       tc_commit(done_qk);
       mbar_wait(done_qk, 0, 100000000ull);
-    } else {
+    } else if constexpr (!F8) {   // (with an fp8 pool the softmax threads write Q)
       // Each unit's Q tile, once every QK^T of the previous unit has completed: vector i of the tile
       // (v = 128 mt + i, row v / G, head v % G of the KV head) into row i of the 128-byte-swizzled
       // K-major atoms, 16 bytes a copy; rows past the last vector are zero. These 31 lanes run apart
@@ -461,7 +586,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // one MMA covers every output column: the two V halves of a d = 256 tile sit in adjacent
       // ring slots (even ring ordinals, an even ring length), so their four 64-column atoms are
       // 8 KB apart throughout
-      constexpr uint32_t kIdescO = mma_idesc(kMmaM, D, true, PvF16);
+      constexpr uint32_t kIdescO = mma_idesc(kMmaM, D, true, F8);   // bf16, or E4M3 (format 0)
+      constexpr int kStep = F8 ? 32 : 16;                           // positions of one MMA's K
       TileIter it;
       it.begin(p, m_tiles, n_units, HI);
       bool ok = true;
@@ -474,25 +600,31 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         for (int j = 0; j < HI && ok; ++j) ok = bwait(&vfull[(vi + j) % NV], ((vi + j) / NV) & 1u, abort_flag);
         if (!ok) break;
         const int valid = min(kMmaN, it.mu.end - (it.mu.start + it.t * kMmaN));
-        const int ksteps = (valid + 15) >> 4;
+        const int ksteps = (valid + kStep - 1) / kStep;
         char* vd = vring + (vi % NV) * kSlotBytes;
-        if (valid & 15) {   // V rows past the split's end inside the last 16-position step: zeros
+        if (valid % kStep) {   // V rows past the split's end inside the last K step: zeros
           const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          for (int at = 0; at < 2 * HI; ++at)
-            for (int rr = valid; rr < (ksteps << 4); ++rr)
-              for (int e = 0; e < 8; ++e) *reinterpret_cast<uint4*>(vd + at * (kMmaN * 128) + rr * 128 + e * 16) = z;
+          for (int at = 0; at < (F8 ? D / 128 : 2 * HI); ++at)
+            for (int rr = valid; rr < ksteps * kStep; ++rr)
+              for (int e = 0; e < 8; ++e) *reinterpret_cast<uint4*>(vd + at * kAtomBytes + rr * 128 + e * 16) = z;
           fence_proxy_async();
         }
         tc_fence_after();
         const uint32_t pcol = tmem + sy * kMmaN;
         const uint32_t vb = smem_u32(vd);
+        // P_hi, then P_lo: K steps of kStep positions, 8 TMEM columns each (two bf16 or four E4M3
+        // codes a column); the V atoms of one tile are kAtomBytes apart throughout
 #pragma unroll
-        for (int part = 0; part < (PvF16 ? 1 : 2); ++part) {   // P_hi, then P_lo (or the one f16 P)
+        for (int part = 0; part < 2; ++part) {
 #pragma unroll
-          for (int kk = 0; kk < kMmaN / 16; ++kk) {
-            if (kk < ksteps)
-              tc_mma_ts(tmem + C::kOCol, pcol + part * (kMmaN / 2) + kk * 8, smem_desc(vb + kk * (16 * 128), kMmaN * 128, 1024),
-                        kIdescO, !(it.t == 0 && part == 0 && kk == 0));
+          for (int kk = 0; kk < kMmaN / kStep; ++kk) {
+            if (kk < ksteps) {
+              const uint32_t acol = pcol + part * (F8 ? kMmaN / 4 : kMmaN / 2) + kk * 8;
+              const uint64_t bd = smem_desc(vb + kk * (kStep * 128), kAtomBytes, 1024);
+              const bool acc = !(it.t == 0 && part == 0 && kk == 0);
+              if constexpr (F8) tc_mma_ts_f8(tmem + C::kOCol, acol, bd, kIdescO, acc);
+              else tc_mma_ts(tmem + C::kOCol, acol, bd, kIdescO, acc);
+            }
           }
         }
         for (int j = 0; j < HI; ++j) tc_commit(&vempty[(vi + j) % NV]);
@@ -524,6 +656,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     TileIter it;
     it.begin(p, m_tiles, n_units, HI);
     int pg_cur = it.done ? 0 : chunk_pages(p, it.mu, 0, lane), pg_nxt = 0;   // lane l: page of tile 32c + l
+    float q_inv = 1.f;   // fp8 pools: 2^-e of this thread's query vector in the unit's Q terms
+    if constexpr (F8) {
+      if (!it.done) {
+        q_inv = q_to_e4m3_terms<D>(p, it.mu, row, q_s);
+        fence_proxy_async();   // the terms are read by the tensor pipe (async proxy)
+        mbar_arrive(q_full);
+      }
+    }
     while (!it.done && ok) {
       const MmaUnit mu = it.mu;
       const int vq = mu.mt * kMmaM + row;            // this thread's query vector of the KV head
@@ -536,10 +676,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // floor((C + 125) / 2), C = 127 - ceil(log2 n) - ceil(log2 256) for the split's n keys, with
       // every |v| <= 256, takes its weights as 2^(z - m) with m = ceil(U) - C fixed before the split is
       // read: no running max, no rescale, and no term overflows or falls below 2^-125. Other rows keep
-      // the online max. P in f16 (the widened fp8 window) cannot hold 2^C: that path is never fixed.
+      // the online max. P in E4M3 (an fp8 pool) cannot hold 2^C: that path is never fixed.
       bool fixed = false;
       float m_fix = 0.f;
-      if (!PvF16 && p.fs_kv_max != nullptr && row_ok) {
+      if (!F8 && p.fs_kv_max != nullptr && row_ok) {
         const int64_t orow = (static_cast<int64_t>(mu.b) * p.rows + r) * p.h_q + static_cast<int64_t>(mu.h) * G + gq;
         const float2 kv = *reinterpret_cast<const float2*>(p.fs_kv_max + 2 * (static_cast<int64_t>(mu.b) * p.h_kv + mu.h));
         const float U = p.fs_q_norm[orow] * kv.x * p.fs_scale_log2;
@@ -549,6 +689,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         m_fix = ceilf(U) - static_cast<float>(Cn);
       }
       float m_run = fixed ? m_fix : -INFINITY, l_run = 0.f;
+      float e_run = 0.f;   // fp8 pools: bound on the terms' absolute floor errors so far (same scale as l)
       uint32_t pb = 0, pp = 0;   // buffer and phase count of the previous tile (g - 1)
       for (int t = 0; t < mu.tiles; ++t) {
         const int n0 = mu.start + t * kMmaN;
@@ -573,7 +714,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
           for (int j = 0; j < kMmaN; ++j) sr[j] = j <= lim ? sr[j] : 0xff800000u;   // -inf
         }
-        const float c = p.qk_scale_log2;
+        const float c = F8 ? p.qk_scale_log2 * q_inv : p.qk_scale_log2;   // 2^-e: exact
         float mx = -INFINITY;
         if (!fixed) {
           float mxa[8];
@@ -588,65 +729,113 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           mx = mxa[0] * c;
         }
         // a NaN running max stays NaN (a later tile the row cannot see, max -inf, must not replace it)
-        const bool grow = !fixed && !(mx <= m_run + kMmaTau) && m_run == m_run;
-        const float m_new = grow ? mx : m_run;
-        const float f = grow ? fast_exp2(m_run - m_new) : 1.f;
-        if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
-          // O holds the PVs of tiles g-t .. g-1: wait for the last, then rescale it in TMEM
-          if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 1
-          for (int cc = 0; cc < D / 16; ++cc) {
-            uint32_t ov[16];
-            tmem_ld16(lane_base + C::kOCol + cc * 16, ov);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-            tmem_st16(lane_base + C::kOCol + cc * 16, ov);
-          }
-        }
-        m_run = m_new;
-        l_run *= f;
-        const float nm = (m_run == -INFINITY) ? 0.f : -m_run;   // all scores -inf: p = 0
-        // ---- p = 2^(s c - m); P_hi = p with the low 16 bits cleared, P_lo = (p - P_hi) likewise:
-        // both exact bf16 values, p - P_hi - P_lo < 2^-14 p. Pairs packed with a byte permute
-        // (upper halves), hi over S columns [0, 32), lo over [32, 64).
+        const bool grow = !fixed && !(mx <= m_run + (F8 ? kF8Hi : kMmaTau)) && m_run == m_run;
+        float m_new = grow ? (F8 ? mx - kF8Mid : mx) : m_run;
+        float f = grow ? fast_exp2(m_run - m_new) : 1.f;
         float ls[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) ls[i] = 0.f;
+        float pv[F8 ? kMmaN : 1];   // fp8 pools: the tile's weights, kept until m is settled
+        float e_tile = 0.f;
+        if constexpr (F8) {
+          const float nm0 = (m_new == -INFINITY) ? 0.f : -m_new;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+          for (int j = 0; j < kMmaN; ++j) {
+            pv[j] = fast_exp2(fmaf(__uint_as_float(sr[j]), c, nm0));
+            ls[j & 7] += pv[j];
+          }
+          // The terms hold each p to 2^-9 p, plus an absolute floor of 2^-9 when p < 2^-1 (E4M3
+          // holds nothing below 2^-9). The floors are kept within 2^-8 of the weight gathered,
+          // l: e_run bounds their sum. A tile adds at most 2^-9 per visible position; only when
+          // that could pass the budget are its weights below 2^-1 counted (branch-free: the sign
+          // of bits(p) - bits(1/2), less the masked columns, exact zeros), and if they still pass
+          // it, m moves down to put the tile's largest weight at 2^kF8Mid, which leaves it at most
+          // 2^-9 of the tile's weight -- unless the weight gathered would pass 2^40 (f = inf
+          // included), when the tile adds less than 2^-25 of the total.
+          const int masked = lim >= kMmaN - 1 ? 0 : kMmaN - 1 - lim;
+          e_tile = 0.001953125f * static_cast<float>(kMmaN - masked);
+          float w_t = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w_t += ls[i];
+          const float budget = 0.00390625f * (l_run * f + w_t);
+          if (e_run * f + e_tile > budget && mx > -INFINITY) {
+            uint32_t n = 0;
+#pragma unroll
+            for (int j = 0; j < kMmaN; ++j) n += (__float_as_uint(pv[j]) - 0x3F000000u) >> 31;
+            e_tile = 0.001953125f * static_cast<float>(static_cast<int>(n) - masked);
+            const float fd = fast_exp2(m_new - (mx - kF8Mid));
+            if (e_run * f + e_tile > budget && fd > 1.f && l_run * f * fd <= kF8MaxWeight) {
+              m_new = mx - kF8Mid;
+              f *= fd;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) ls[i] *= fd;
+#pragma unroll
+              for (int j = 0; j < kMmaN; ++j) pv[j] *= fd;
+              e_tile = 0.001953125f * static_cast<float>(kMmaN - masked);   // <= 2^-9 * 2^kF8Mid
+            }
+          }
+        }
+        const float nm = (m_new == -INFINITY) ? 0.f : -m_new;   // all scores -inf: p = 0
+        // ---- p = 2^(s c - m) as two terms written over the S columns they came from (before any
+        // rescale of O: the product of the previous tile may still run meanwhile)
+        if constexpr (F8) {
+          // E4M3 terms (split4), four codes a column: P_hi over S columns [0, 16), P_lo over [16, 32)
           uint32_t wh[16], wl[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int j = half * 32 + 2 * i;
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j]), c, nm));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), c, nm));
-            ls[j & 7] += p0;
-            ls[(j + 1) & 7] += p1;
-            if constexpr (PvF16) {   // f16, round to nearest: p - P < 2^-11 p (p <= 2^8 fits)
-              const __half2 h = __floats2half2_rn(p0, p1);
-              wh[i] = *reinterpret_cast<const uint32_t*>(&h);
-            } else {
+          for (int i = 0; i < 16; ++i) p_terms4(pv + 4 * i, wh[i], wl[i]);
+          tmem_st16(lane_base + (sbuf - tmem), wh);
+          tmem_st16(lane_base + (sbuf - tmem) + kMmaN / 4, wl);
+        } else {
+          // bf16 terms: P_hi = p with the low 16 bits cleared, P_lo = (p - P_hi) likewise, both exact
+          // bf16 values, p - P_hi - P_lo < 2^-14 p; pairs packed with a byte permute (upper halves),
+          // hi over S columns [0, 32), lo over [32, 64)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t wh[16], wl[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = half * 32 + 2 * i;
+              const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j]), c, nm));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j + 1]), c, nm));
+              ls[j & 7] += p0;
+              ls[(j + 1) & 7] += p1;
               const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
               wh[i] = __byte_perm(u0, u1, 0x7632);
               const float l0 = p0 - __uint_as_float(u0 & 0xffff0000u);
               const float l1 = p1 - __uint_as_float(u1 & 0xffff0000u);
               wl[i] = __byte_perm(__float_as_uint(l0), __float_as_uint(l1), 0x7632);
             }
+            tmem_st16(lane_base + (sbuf - tmem) + half * 16, wh);
+            tmem_st16(lane_base + (sbuf - tmem) + kMmaN / 2 + half * 16, wl);
           }
-          tmem_st16(lane_base + (sbuf - tmem) + half * 16, wh);
-          if constexpr (!PvF16) tmem_st16(lane_base + (sbuf - tmem) + kMmaN / 2 + half * 16, wl);
         }
 #pragma unroll
         for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
           for (int i = 0; i < w; ++i) ls[i] += ls[i + w];
-        const float lsum = ls[0];
-        l_run += lsum;
+        if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
+          // O holds the PVs of tiles g-t .. g-1: wait for the last, then rescale it in TMEM, 64
+          // columns a round with the loads in flight together
+          if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t ov[64];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16(lane_base + C::kOCol + cc * 64 + q * 16, ov + q * 16);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 64; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_st16(lane_base + C::kOCol + cc * 64 + q * 16, ov + q * 16);
+          }
+        }
+        m_run = m_new;
+        l_run = l_run * f + ls[0];
+        if constexpr (F8) e_run = e_run * f + e_tile;
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[gb]);
@@ -660,12 +849,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
       if (!ok) break;
       if (fixed && l_run == 0.f) m_run = -INFINITY;   // no visible key: an empty partial, as online
+      float q_inv_next = 1.f;
+      if constexpr (F8) {
+        // the next unit's Q terms: every QK^T of this unit has completed (its last S was read)
+        if (it.has_next) {
+          q_inv_next = q_to_e4m3_terms<D>(p, it.next_mu(), row, q_s);
+          fence_proxy_async();
+          mbar_arrive(q_full);
+        }
+      }
       // ---- the unit's last PV is done: O is complete
       if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
         ok = false;
         break;
       }
       it.next_unit(p);
+      q_inv = q_inv_next;
       if (!it.done) pg_cur = chunk_pages(p, it.mu, 0, lane);
       // ---- epilogue: O from TMEM. Each thread stores its own row, 32 columns at a time, straight
       // from registers with 32-byte stores: every store fills whole 32-byte sectors, and nothing
@@ -673,8 +872,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       tc_fence_after();
       const bool single = mu.n_splits <= 1;
       const float sc = single ? ((m_run == -INFINITY) ? 0.f : p.v_scale / l_run) : 1.f;
-      // f16 partials (fp8 windows): acc / l, which stays within the E4M3 codes' range
-      const bool half_part = PvF16 && p.part_f16 && !single;
+      // f16 partials (fp8 pools): acc / l, which stays within the E4M3 codes' range
+      const bool half_part = F8 && p.part_f16 && !single;
       const float il = (m_run == -INFINITY) ? 0.f : 1.f / l_run;
       float* dst = nullptr;
       if (row_ok) {
@@ -758,18 +957,19 @@ bool encode(CUtensorMap* map, CUtensorMapDataType type, int rank, const void* ba
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_maps(MmaMaps* m, const DecodeParams& p, bool v_f16) {
+bool make_maps(MmaMaps* m, const DecodeParams& p, bool f8) {
   const cuuint64_t D = static_cast<cuuint64_t>(p.d);
-  // pools: rows (page * h_kv + h) * page_tokens + position, columns d
+  // pools: rows (page * h_kv + h) * page_tokens + position, columns d; a box is 64 positions of
+  // 128 bytes (64 bf16 or 128 E4M3 codes)
   const cuuint64_t pool_dims[2] = {D, static_cast<cuuint64_t>(p.num_pages) * p.h_kv * p.page_tokens};
-  const cuuint64_t pool_str[1] = {D * 2};
-  const cuuint32_t pool_box[2] = {64, static_cast<cuuint32_t>(kMmaN)};
-  if (!encode(&m->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.k_pool, pool_dims, pool_str, pool_box) ||
-      !encode(&m->v, v_f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.v_pool,
-              pool_dims, pool_str, pool_box))
+  const cuuint64_t pool_str[1] = {D * (f8 ? 1 : 2)};
+  const cuuint32_t pool_box[2] = {f8 ? 128u : 64u, static_cast<cuuint32_t>(kMmaN)};
+  const CUtensorMapDataType pool_type = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode(&m->k, pool_type, 2, p.k_pool, pool_dims, pool_str, pool_box) ||
+      !encode(&m->v, pool_type, 2, p.v_pool, pool_dims, pool_str, pool_box))
     return false;
   const int rt = whole_row_tile_rows(p.rows, p.group);
-  if (rt == 0) return true;
+  if (f8 || rt == 0) return true;   // Q is written by threads
   // q [B][R][h_q][d] bf16
   const cuuint64_t HQ = static_cast<cuuint64_t>(p.h_q), R = static_cast<cuuint64_t>(p.rows);
   const cuuint64_t q_dims[4] = {D, HQ, R, static_cast<cuuint64_t>(p.batch)};
@@ -778,17 +978,17 @@ bool make_maps(MmaMaps* m, const DecodeParams& p, bool v_f16) {
   return encode(&m->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.q, q_dims, q_str, q_box);
 }
 
-template <int D, bool PvF16>
+template <int D, bool F8>
 cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
-  using C = MmaCfg<D>;
+  using C = MmaCfg<D, F8>;
   static std::atomic<uint64_t> configured{0};   // devices whose shared-memory limit is raised
   MmaMaps maps;
-  if (!make_maps(&maps, p, PvF16)) return cudaErrorInvalidValue;
+  if (!make_maps(&maps, p, F8)) return cudaErrorInvalidValue;
   const DeviceInfo& di = device_info();
   const uint64_t bit = 1ull << (di.device & 63);
   if ((configured.load() & bit) == 0) {
     const cudaError_t e =
-        cudaFuncSetAttribute(decode_partial_mma_kernel<D, PvF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(decode_partial_mma_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
@@ -799,7 +999,7 @@ cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t strea
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
-  return launch_pdl(decode_partial_mma_kernel<D, PvF16>, static_cast<unsigned>(grid), kMmaThreads, C::kSmem,
+  return launch_pdl(decode_partial_mma_kernel<D, F8>, static_cast<unsigned>(grid), kMmaThreads, C::kSmem,
                     stream, p, maps);
 }
 
@@ -807,99 +1007,18 @@ cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t strea
 
 bool mma_path_applies(const DecodeParams& p, int q_dtype, int pool_dtype) {
   const int64_t pool_rows = static_cast<int64_t>(p.num_pages) * p.h_kv * p.page_tokens;
-  return q_dtype == NBX_BF16 && pool_dtype == NBX_BF16 && (p.d == 128 || p.d == 256) &&
+  return q_dtype == NBX_BF16 && (pool_dtype == NBX_BF16 || pool_dtype == NBX_E4M3) && (p.d == 128 || p.d == 256) &&
          (p.page_tokens % kMmaN) == 0 && p.group <= kMmaM && p.rows * p.group >= 64 &&
          pool_rows < (int64_t{1} << 31) - kMmaN && p.qk_scale_log2 > 0.f;
 }
 
-cudaError_t decode_dispatch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
+cudaError_t decode_dispatch_mma(const DecodeParams& p, int pool_dtype, int grid_limit, cudaStream_t stream) {
+  if (pool_dtype == NBX_E4M3) {
+    if (p.d == 128) return launch_mma<128, true>(p, grid_limit, stream);
+    return launch_mma<256, true>(p, grid_limit, stream);
+  }
   if (p.d == 128) return launch_mma<128, false>(p, grid_limit, stream);
   return launch_mma<256, false>(p, grid_limit, stream);
 }
-
-// ---- fp8 pools: bf16 copies of the sequences for the tensor-core kernel
-namespace {
-
-constexpr int kWidenThreads = 256;
-
-// One CTA per (sequence b, 64-position page t of the copies, KV head h): the E4M3 codes of K and V
-// at positions 64t .. 64t + 63 (up to the sequence's length), read through the block table and
-// written into the copies, K as bf16 and V as f16 -- exactly, since every E4M3 value (3 mantissa
-// bits, magnitudes 2^-9 .. 448) is both a bf16 and an f16 value. The page's
-// table entry is its own index, or -1 when the source page id is outside the pool (its positions
-// then stay masked, as the SIMT kernel skips them). Pages past the length are not touched.
-__global__ void __launch_bounds__(kWidenThreads) widen_kernel(DecodeParams p) {
-  pdl_wait();   // the plan kernel's lengths and the append's positions are visible from here on
-  pdl_launch_dependents();
-  const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.h_kv));
-  const int64_t pg = blockIdx.x / static_cast<unsigned>(p.h_kv);   // b * t64 + t
-  const int b = static_cast<int>(pg / p.t64);
-  const int t = static_cast<int>(pg - static_cast<int64_t>(b) * p.t64);
-  const int L = p.plan[b].len;
-  const int n0 = t * 64;
-  if (n0 >= L) return;
-  const int page = p.block_table[static_cast<int64_t>(b) * p.max_pages + n0 / p.page_tokens];
-  const bool page_ok = page >= 0 && page < p.num_pages;
-  if (threadIdx.x == 0 && h == 0) {
-    p.widen_bt[pg] = page_ok ? static_cast<int32_t>(pg) : -1;
-    if (!page_ok) raise_status(p.status, NBX_DEV_BAD_PAGE);
-  }
-  if (!page_ok) return;
-  const int rows = min(64, L - n0);
-  const int cpr = p.d / 16;   // 16-byte chunks of codes per position
-  const int64_t src_row = (static_cast<int64_t>(page) * p.h_kv + h) * p.page_tokens + (n0 % p.page_tokens);
-  const int64_t dst_row = (pg * p.h_kv + h) * 64;
-  for (int kv = 0; kv < 2; ++kv) {
-    const uint8_t* src = static_cast<const uint8_t*>(kv == 0 ? p.k_pool : p.v_pool) + src_row * p.d;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(kv == 0 ? p.widen_k : p.widen_v) + dst_row * p.d * 2);
-    for (int c = threadIdx.x; c < rows * cpr; c += kWidenThreads) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(c) * 16);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 lo = e4m3x2_to_float2(w[i] & 0xffffu);
-        const float2 hi = e4m3x2_to_float2(w[i] >> 16);
-        if (kv == 0) {   // K: bf16, the format of Q in QK^T
-          const __nv_bfloat162 a = __floats2bfloat162_rn(lo.x, lo.y);
-          const __nv_bfloat162 bb = __floats2bfloat162_rn(hi.x, hi.y);
-          o[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
-          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bb);
-        } else {         // V: f16, so P can enter PV as one f16 term
-          const __half2 a = __floats2half2_rn(lo.x, lo.y);
-          const __half2 bb = __floats2half2_rn(hi.x, hi.y);
-          o[2 * i] = *reinterpret_cast<const uint32_t*>(&a);
-          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&bb);
-        }
-      }
-      dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
-      dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-    }
-  }
-}
-
-}  // namespace
-
-bool widen_path_applies(int q_dtype, int pool_dtype, int rows, int h_q, int h_kv, int d, int page_tokens) {
-  const int group = h_q / h_kv;
-  return q_dtype == NBX_BF16 && pool_dtype == NBX_E4M3 && (d == 128 || d == 256) && (page_tokens % kMmaN) == 0 &&
-         group <= kMmaM && rows * group >= 64;
-}
-
-cudaError_t decode_dispatch_widened(const DecodeParams& p, int grid_limit, cudaStream_t stream) {
-  const int64_t blocks = static_cast<int64_t>(p.batch) * p.t64 * p.h_kv;
-  cudaError_t e = launch_pdl(widen_kernel, static_cast<unsigned>(blocks), kWidenThreads, 0, stream, p);
-  if (e != cudaSuccess) return e;
-  DecodeParams w = p;   // the tensor-core kernel on the copies: 64-position pages, identity table
-  w.k_pool = p.widen_k;
-  w.v_pool = p.widen_v;
-  w.block_table = p.widen_bt;
-  w.max_pages = p.t64;
-  w.page_tokens = kMmaN;
-  w.num_pages = p.batch * p.t64;
-  if (w.d == 128) return launch_mma<128, true>(w, grid_limit, stream);
-  return launch_mma<256, true>(w, grid_limit, stream);
-}
-
 
 }  // namespace nbx

@@ -70,18 +70,13 @@ struct WorkspaceLayout {
   size_t m_part;    // f32[batch * rows * h_q * max_splits]   (log2 units)
   size_t l_part;    // f32[batch * rows * h_q * max_splits]
   size_t acc_part;  // f32[batch * rows * h_q * max_splits * d]
-  // bf16 copies of an fp8 pool's sequences for the tensor-core kernel (present only when asked
-  // for): [batch * t64][h_kv][64][d] for K and for V, and their page table int32[batch][t64]
-  size_t widen_k, widen_v, widen_bt;
   size_t total;
-  int t64;          // 64-position pages per sequence in the copies (0: no copies)
   int max_splits;
   int row_blocks;
 };
 
 // Returns false if the sizes overflow.
-bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* out,
-                      bool widen = false);
+bool workspace_layout(int batch, int rows, int h_q, int h_kv, int d, int max_seq_len, WorkspaceLayout* out);
 
 int splits_for(int length);
 
@@ -104,11 +99,6 @@ struct DecodeParams {
   int max_splits, row_blocks;
   float qk_scale_log2;  // scale * k_scale * log2(e): scores in log2 units
   float v_scale;
-  // bf16 copies of an fp8 pool for the tensor-core kernel (null: none)
-  void* widen_k;
-  void* widen_v;
-  int32_t* widen_bt;
-  int t64;
   // the plan kernel writes ident_bt[b] = b (a contiguous cache read as one page per sequence;
   // block_table then points at it), and, for a decode step, attends with seq_lens[b] + len_add
   // and writes that length to lens_out[b] (null: neither)
@@ -130,7 +120,7 @@ struct DecodeParams {
   float fs_scale_log2;
   float k_scale_host;   // the pool's k scale (the bounds kernel reports |k| dequantised)
   // split partials as f16 acc / l (the partial normalised by its own sum) instead of fp32 acc: set
-  // for fp8 windows on tensor cores, where acc / l is a convex combination of E4M3 codes (|code|
+  // for fp8 pools on tensor cores, where acc / l is a convex combination of E4M3 codes (|code|
   // <= 448, the v scale is applied by the merge), so f16 neither overflows nor loses more than
   // 2^-11 relative; each (row, split) slot holds d halves in the first half of its d floats
   int part_f16;
@@ -148,18 +138,11 @@ cudaError_t bounds_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
 cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, int grid_limit, cudaStream_t stream);
 
 // The tensor-core partial kernel: used when the query vectors of one KV head fill an MMA tile
-// (rows x group >= 64), q and pools are bf16, d is 128 or 256 and pages hold a multiple of 64
-// positions.
+// (rows x group >= 64), q is bf16, the pools bf16 (kind::f16) or E4M3 (kind::f8f6f4 on the codes),
+// d is 128 or 256 and pages hold a multiple of 64 positions.
 bool mma_path_applies(const DecodeParams& p, int q_dtype, int pool_dtype);
 constexpr int kMmaRowsPerTile = 128;   // query vectors of one M tile of the tensor-core kernel
-cudaError_t decode_dispatch_mma(const DecodeParams& p, int grid_limit, cudaStream_t stream);
-
-// fp8 pools with a multi-row window: the same tensor-core kernel runs on bf16 copies of the
-// sequences' K/V, widened into the workspace (every E4M3 value is a bf16 value, so the copies are
-// exact). The copies use 64-position pages [batch * t64][h_kv][64][d]; a page whose source page id
-// is outside the pool is marked -1, so its positions stay masked.
-bool widen_path_applies(int q_dtype, int pool_dtype, int rows, int h_q, int h_kv, int d, int page_tokens);
-cudaError_t decode_dispatch_widened(const DecodeParams& p, int grid_limit, cudaStream_t stream);
+cudaError_t decode_dispatch_mma(const DecodeParams& p, int pool_dtype, int grid_limit, cudaStream_t stream);
 
 // Launch with programmatic dependent launch: the grid may start while the previous kernel in the
 // stream finishes; the kernel orders itself after it with griddepcontrol.wait.

@@ -1,6 +1,6 @@
 // tcgen05 (fifth-generation tensor core) and TMA wrappers in inline PTX, shared by the tensor-core
 // decode kernels: TMEM allocation, MMA issue and completion, TMEM loads and stores, tensor-map
-// copies, and the shared-memory and instruction descriptors of kind::f16 MMAs.
+// copies, and the shared-memory and instruction descriptors of kind::f16 and kind::f8f6f4 MMAs.
 #pragma once
 
 #include <cstdint>
@@ -49,6 +49,28 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+
+// The same two forms with kind::f8f6f4: 8-bit operands (E4M3 both, by the instruction descriptor),
+// K = 32 a step; from TMEM, four elements of K per 32-bit column (the lowest K index in the lowest
+// byte).
+__device__ __forceinline__ void tc_mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
       : "memory");
 }
@@ -105,10 +127,11 @@ __device__ __forceinline__ void st_global_v8_hint(float* dst, const float (&v)[8
 // Shared-memory matrix descriptor: start >> 4 in bits [0,14), leading byte offset >> 4 in [16,30),
 // stride byte offset >> 4 in [32,46), descriptor version 1 in [46,48), base offset 0 (operand
 // blocks are 1024-byte aligned), layout 2 = 128-byte swizzle in [61,64).
-//   K-major, 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row groups 1024 bytes apart
-//     (stride offset); a K step of 16 elements advances the start by 32 bytes.
-//   MN-major, 128-byte swizzle: rows of 128 bytes (64 bf16 of N) per K index, 8-K groups 1024
-//     bytes apart (stride offset), 64-wide N blocks `lbo` bytes apart (leading offset).
+//   K-major, 128-byte swizzle: rows of 128 bytes (64 bf16 or 128 E4M3 of K), 8-row groups 1024
+//     bytes apart (stride offset); a K step (16 bf16, 32 E4M3) advances the start by 32 bytes.
+//   MN-major, 128-byte swizzle: rows of 128 bytes (64 bf16 or 128 E4M3 of N) per K index, 8-K
+//     groups 1024 bytes apart (stride offset), 128-byte-wide N blocks `lbo` bytes apart (leading
+//     offset).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
@@ -116,7 +139,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B both bf16 (bits 7-9
 // and 10-12 = 1) or both f16 (0), A K-major or MN-major (bit 15), B K-major or MN-major (bit 16),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28. With kind::f8f6f4 the same formats field 0 means
+// E4M3 for both operands.
 __host__ __device__ constexpr uint32_t mma_idesc(int m, int n, bool b_mn_major, bool f16 = false,
                                                  bool a_mn_major = false) {
   const uint32_t fmt = f16 ? 0u : 1u;

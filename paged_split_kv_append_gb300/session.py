@@ -32,8 +32,7 @@ def new_pool(num_pages: int, h_kv: int, page_tokens: int, d: int, dtype: str, de
 
 class PagedDecodeSession:
     def __init__(self, *, num_pages: int, h_kv: int, page_tokens: int, d: int, pool_dtype: str, batch: int,
-                 rows: int, h_q: int, max_seq_len: int, device, fill_nan: bool = True, q_dtype: str = "bf16",
-                 widen: bool = True):
+                 rows: int, h_q: int, max_seq_len: int, device, fill_nan: bool = True, q_dtype: str = "bf16"):
         self.device = torch.device(device)
         self.num_pages, self.h_kv, self.page_tokens, self.d = num_pages, h_kv, page_tokens, d
         self.pool_dtype = pool_dtype
@@ -41,9 +40,8 @@ class PagedDecodeSession:
         self.k_pool = new_pool(num_pages, h_kv, page_tokens, d, pool_dtype, self.device, fill_nan)
         self.v_pool = new_pool(num_pages, h_kv, page_tokens, d, pool_dtype, self.device, fill_nan)
         codes = {"f32": NBX_F32, "bf16": NBX_BF16, "e4m3": NBX_E4M3}
-        # widen=False sizes the workspace without the bf16 copies an fp8 pool can use on tensor cores
-        ws = nbx_paged_decode_workspace_bytes_for(codes[q_dtype], codes[pool_dtype] if widen else NBX_F32, batch,
-                                                  rows, h_q, h_kv, d, max_seq_len, page_tokens)
+        ws = nbx_paged_decode_workspace_bytes_for(codes[q_dtype], codes[pool_dtype], batch, rows, h_q, h_kv, d,
+                                                  max_seq_len, page_tokens)
         if ws == 0 and batch > 0:
             raise ValueError("invalid decode sizes")
         self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.device)

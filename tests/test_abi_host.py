@@ -198,15 +198,18 @@ def test_partial_kernel_choice(lib):
             (nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 256, 2 ** 23, 64)]  # pool rows beyond 2^31 - 64
     for args in simt:
         assert nbx.nbx_paged_decode_partial_kernel(*args) == nbx.PARTIAL_SIMT, args
-    # fp8 pool with a multi-row window: tensor cores on bf16 copies, which the larger workspace holds
+    # fp8 pool with a multi-row window: tensor cores on the codes (bf16 q only), no extra workspace
     assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, 128, 24, 4, 256, 1000, 64) == \
-        nbx.PARTIAL_TCGEN05_WIDENED
+        nbx.PARTIAL_TCGEN05_FP8
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, 16, 24, 4, 128, 1000, 128) == \
+        nbx.PARTIAL_TCGEN05_FP8
     assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_F32, nbx.NBX_E4M3, 128, 24, 4, 256, 1000, 64) == \
         nbx.PARTIAL_SIMT
+    assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, 8, 24, 4, 256, 1000, 64) == \
+        nbx.PARTIAL_SIMT   # 48 query vectors
     base = nbx.nbx_paged_decode_workspace_bytes(1, 128, 24, 4, 256, 32768)
-    widened = nbx.nbx_paged_decode_workspace_bytes_for(nbx.NBX_BF16, nbx.NBX_E4M3, 1, 128, 24, 4, 256, 32768, 64)
-    assert widened >= base + 2 * 32768 * 4 * 256 * 2
-    assert nbx.nbx_paged_decode_workspace_bytes_for(nbx.NBX_BF16, nbx.NBX_BF16, 1, 128, 24, 4, 256, 32768, 64) == base
+    for qd, pd in ((nbx.NBX_BF16, nbx.NBX_E4M3), (nbx.NBX_BF16, nbx.NBX_BF16), (nbx.NBX_F32, nbx.NBX_F32)):
+        assert nbx.nbx_paged_decode_workspace_bytes_for(qd, pd, 1, 128, 24, 4, 256, 32768, 64) == base
     assert lib.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 5, 256, 10, 64) == -2
     assert lib.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_BF16, 16, 24, 4, 256, 10, 40) == -4
     assert lib.nbx_paged_decode_partial_kernel(7, nbx.NBX_BF16, 16, 24, 4, 256, 10, 64) == -3

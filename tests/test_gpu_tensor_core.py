@@ -1,9 +1,10 @@
 """GPU parity of the tensor-core split partial (tcgen05) against the float64 oracle.
 
 The decode runs this kernel when the query vectors of one KV head fill an MMA tile
-(rows x group >= 64, bf16 q and pools, d 128 or 256, pages of a multiple of 64 positions):
-multi-row verify windows and prefill chunks. Same bars as the SIMT kernel: max |err| 2e-3 for
-bf16 pools, bit-identical under page relabelling, grid size and batch order; pools start as NaN.
+(rows x group >= 64, bf16 q, bf16 or E4M3 pools, d 128 or 256, pages of a multiple of 64
+positions): multi-row verify windows and prefill chunks. Same bars as the SIMT kernel: max |err|
+2e-3 for bf16 pools and 3e-2 for E4M3 pools, bit-identical under page relabelling, grid size and
+batch order; pools start as NaN.
 """
 
 import numpy as np
@@ -129,26 +130,90 @@ def test_one_cta_runs_every_unit(d, h_q, h_kv, page):
 def fp8_config(name, lens, seed, rows=16, page=64):
     cfg = wl.Config(name, len(lens), rows, 24, 4, 256, page, "e4m3", "bf16", seed, ("fixed", tuple(lens)))
     kind = nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, rows, 24, 4, 256, 1000, page)
-    assert kind == nbx.PARTIAL_TCGEN05_WIDENED
+    assert kind == nbx.PARTIAL_TCGEN05_FP8
     return cfg
 
 
-def test_fp8_pool_window_on_widened_copies():
-    # the copies are exact, so the tensor-core result is held to the bf16 bound, and it agrees with
-    # the SIMT kernel that runs when the workspace has no room for the copies
+def test_fp8_pool_window_on_the_codes():
+    # kind::f8f6f4 on the stored codes, Q and P as two E4M3 terms each: held to the fp8 bound
     cfg = fp8_config("tc_fp8", (1, 64, 100, 700, 1500), 36)
     case = wl.make_case(cfg, device=DEV)
     sess, out = run_step(case)
-    err = check_against_oracle(case, sess, out)
-    assert err <= 2e-3, err
-    simt = bench.session_for_case(case, DEV, widen=False)
-    out_simt = simt.step().clone()
-    torch.cuda.synchronize()
-    assert simt.status_bits() == 0
-    assert float((out - out_simt).abs().max()) <= 2e-3
+    check_against_oracle(case, sess, out)
 
 
-def test_fp8_widened_grid_limits_are_bit_exact():
+def fp8_scored_case(name, lens, seed, score_log2):
+    """An fp8 window whose query vectors are all one vector q0 (every row and head) and whose key j
+    is t_j q0 / |q0|^2 in every KV head, t_j set so that the score of position j is score_log2(j)
+    in log2 units (up to the E4M3 rounding of the keys): the score pattern is placed position by
+    position."""
+    cfg = fp8_config(name, lens, seed)
+    case = wl.make_case(cfg, device=DEV)
+    case.q[:] = case.q[0, 0, 0]
+    q0 = case.q[0, 0, 0].float()
+    for b in range(cfg.batch):
+        off, n = int(case.tok_offset[b]), int(case.lens[b])
+        t = torch.tensor([score_log2(b, j, n) for j in range(n)], dtype=torch.float32, device=q0.device)
+        t = t / (case.scale * np.log2(np.e))
+        case.k_raw[off:off + n] = (t[:, None] * q0 / (q0 @ q0))[:, None, :]
+    return wl.Case(**{**case.__dict__, "k_scale": float(case.k_raw.abs().max()) / wl.E4M3_MAX,
+                      "v_scale": float(case.v_raw.abs().max()) / wl.E4M3_MAX})
+
+
+def test_fp8_attention_sink_with_heavy_tail():
+    # One key 10 log2 units above 1,500 others at ~0: each of those weighs ~2^-10 of the sink, below
+    # what one E4M3 term holds next to it, yet together they outweigh it. The running max moves
+    # back down after the sink's tile so their weights keep their bits. The sink sits in the first
+    # tile of sequence 0 and in the middle of sequence 1.
+    def score(b, j, n):
+        return 10.0 if j == (3 if b == 0 else n // 2) else 0.05 * np.sin(0.7 * j)
+    case = fp8_scored_case("tc_fp8_sink", (1500, 1700), 41, score)
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+    # the tail matters: attending to the sink alone would be far off
+    kp, vp = pins.oracle_pools(case)
+    want = pins.oracle_output(case)
+    off = int(case.tok_offset[0])
+    v_sink = case.v_raw[off + 3].float().cpu().numpy()   # ~ the dequantised sink value row of each KV head
+    assert np.max(np.abs(want[0, 0, 0] - v_sink[0])) > 0.2
+
+
+def test_fp8_flat_tail_far_below_a_sink():
+    # Every query vector is e_0 and key j is t_j e_0, so a score is t_j * scale exactly (the sink's
+    # key is the pool's largest, code 448): a sink 14.415 log2 units above 5,999 zero-score keys.
+    # With m 6 below the sink each tail weight is 2^-8.415 = 1.498 * 2^-9, which the E4M3 terms
+    # round to 2^-8 (+33 %), the same way for every key. The tail holds a fifth of the weight and
+    # its values are all +3 (the sink's -3). A window of 128 rows over 6,000 keys is cut into
+    # splits of 1,024: an output that kept the sink split's tail weights would be off by ~0.1.
+    # The floor budget moves m down after two tail tiles, after which the tail's weights keep
+    # their bits (off by ~0.014).
+    cfg = fp8_config("tc_fp8_flat", (6000,), 43, rows=128)
+    case = wl.make_case(cfg, device=DEV)
+    case.q.zero_()
+    case.q[..., 0] = 1.0
+    b_sink = 14.415 / (case.scale * np.log2(np.e))
+    case.k_raw.zero_()
+    case.v_raw.fill_(3.0)
+    for b in range(cfg.batch):
+        sink = int(case.tok_offset[b]) + 3
+        case.k_raw[sink, :, 0] = b_sink
+        case.v_raw[sink] = -3.0
+    case = wl.Case(**{**case.__dict__, "k_scale": b_sink / wl.E4M3_MAX, "v_scale": 3.0 / wl.E4M3_MAX})
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+
+
+@pytest.mark.parametrize("slope", [-2.0, -40.0, 2.0])
+def test_fp8_score_ramps(slope):
+    # scores changing by `slope` log2 units per 64-position tile: falling ramps move the running max
+    # down tile after tile until the gathered weight reaches its bound (-2: gently; -40: at once),
+    # a rising one moves it up
+    case = fp8_scored_case("tc_fp8_ramp", (1400, 900), 42, lambda b, j, n: slope * j / 64.0)
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+
+
+def test_fp8_grid_limits_are_bit_exact():
     cfg = fp8_config("tc_fp8_grid", (130, 1500, 64), 37, rows=32)
     case = wl.make_case(cfg, device=DEV)
     _, ref = run_step(case)
@@ -158,7 +223,7 @@ def test_fp8_widened_grid_limits_are_bit_exact():
         assert torch.equal(out, ref), f"grid limit {limit}"
 
 
-def test_fp8_widened_missing_page_and_nan_code():
+def test_fp8_missing_page_and_nan_code():
     cfg = fp8_config("tc_fp8_bad", (900, 1300), 38)
     case = wl.make_case(cfg, device=DEV)
     case.k_raw[int(case.tok_offset[0]) + 500, 2, 7] = float("nan")   # stored as the E4M3 NaN code
@@ -177,7 +242,7 @@ def test_fp8_widened_missing_page_and_nan_code():
     ref = op.decode_attention(case.q.float().cpu().numpy()[:1], kp, vp, "e4m3", case.block_table[:1], case.lens[:1],
                               cfg.page_tokens, case.scale, case.k_scale, case.v_scale)
     keep = np.isfinite(ref)
-    assert np.max(np.abs(o[:1][keep] - ref[keep])) <= 2e-3
+    assert np.max(np.abs(o[:1][keep] - ref[keep])) <= 3e-2
 
 
 def test_nan_key_reaches_rows_whose_later_tiles_are_masked():
@@ -189,7 +254,7 @@ def test_nan_key_reaches_rows_whose_later_tiles_are_masked():
     case.k_raw[1300, 1, 9] = float("nan")
     sess = bench.session_for_case(case, DEV)
     assert nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, 128, 24, 4, 256, 1, 64) == \
-        nbx.PARTIAL_TCGEN05_WIDENED
+        nbx.PARTIAL_TCGEN05_FP8
     out = sess.step().clone()
     torch.cuda.synchronize()
     assert sess.status_bits() == 0

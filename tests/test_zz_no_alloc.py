@@ -48,7 +48,7 @@ def _call(f, sess, out, status):
 @pytest.mark.parametrize("name,kernel", [("single_row", nbx.PARTIAL_SIMT), ("ragged_small", nbx.PARTIAL_SIMT),
                                          ("tiny", nbx.PARTIAL_SIMT),
                                          ("verify_small", nbx.PARTIAL_TCGEN05),
-                                         ("prefill_small", nbx.PARTIAL_TCGEN05_WIDENED)])
+                                         ("prefill_small", nbx.PARTIAL_TCGEN05_FP8)])
 def test_noalloc_decode_matches_the_workspace_decode_twice(name, kernel):
     # the same kernels with the same plan as the workspace entry point: the outputs are equal bit for bit
     nbx.build()
