@@ -373,7 +373,7 @@ def pack_inputs(sess, dev):
 
 def time_fixed_shift(sess, steps: int, flush, sink, stream):
     """The fixed-shift ablation of a tensor-core window: its bounds pass and the decode call with the
-    bounds (precomputed outside the timed decode), each timed like the decode call."""
+    bounds (precomputed outside the timed decode), each timed like the decode call (graph replays)."""
     import paged_split_kv_append_gb300 as nbx
     with torch.cuda.stream(stream):
         qn, kv = nbx.nbx_paged_decode_bounds(sess.q, sess.k_pool, sess.v_pool, sess.block_table, sess.seq_lens,
@@ -393,11 +393,14 @@ def time_fixed_shift(sess, steps: int, flush, sink, stream):
         out = {}
         for name, fn in (("fixed_shift_decode_us", fixed), ("bounds_us", bounds)):
             fn()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
             for a, b in evs:
                 flush_l2(flush, sink)
                 a.record(stream)
-                fn()
+                g.replay()
                 b.record(stream)
             stream.synchronize()
             out[name] = round(sum(a.elapsed_time(b) for a, b in evs) / steps * 1e3, 3)
@@ -408,8 +411,10 @@ def time_fixed_shift(sess, steps: int, flush, sink, stream):
 
 def time_case(case, dev, steps: int, warmup: int, flush, sink, stream, e2e_steps: int = 0):
     """Time one workload's step (a CUDA-graph replay of append + decode) and its decode call alone
-    (plan + partial + merge, eager), each with the L2 flushed before every timed iteration; with
-    e2e_steps, also the step end to end through the public API with host buffers."""
+    (plan + partial + merge: a CUDA-graph replay, the device time of the three kernels, and the same
+    call launched eagerly, which adds the host's launch gaps), each with the L2 flushed before every
+    timed iteration; with e2e_steps, also the step end to end through the public API with host
+    buffers."""
     sess = session_for_case(case, dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -421,8 +426,12 @@ def time_case(case, dev, steps: int, warmup: int, flush, sink, stream, e2e_steps
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         sess.step(stream=stream)
+    dgraph = torch.cuda.CUDAGraph()          # the decode call alone
+    with torch.cuda.graph(dgraph, stream=stream):
+        sess.decode(stream=stream)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with torch.cuda.stream(stream):
         for i in range(steps):
             flush_l2(flush, sink)
@@ -432,19 +441,26 @@ def time_case(case, dev, steps: int, warmup: int, flush, sink, stream, e2e_steps
         for i in range(steps):               # the decode call alone, same flush discipline
             flush_l2(flush, sink)
             kev[i][0].record(stream)
-            sess.decode(stream=stream)
+            dgraph.replay()
             kev[i][1].record(stream)
+        for i in range(steps):               # and launched eagerly
+            flush_l2(flush, sink)
+            eev[i][0].record(stream)
+            sess.decode(stream=stream)
+            eev[i][1].record(stream)
     stream.synchronize()
     if sess.status_bits() != 0:
         raise RuntimeError(f"device status {sess.status_bits():#x} after the timed steps")
     step_ms = [a.elapsed_time(b) for a, b in ev]
     dec_ms = [a.elapsed_time(b) for a, b in kev]
+    eager_ms = [a.elapsed_time(b) for a, b in eev]
     # our kernels per call: append (when the step has new tokens), plan, partial, and the merge when
     # some sequence can have more than one split
     decode_launches = 2 + (1 if case.max_seq_len > 256 else 0)
     step_launches = decode_launches + (1 if (sess.new_k is not None and sess.new_k.shape[0] > 0) else 0)
     r = dict(step_ms=step_ms, ms_per_step=sum(step_ms) / len(step_ms), dec_ms=sum(dec_ms) / len(dec_ms),
-             launches=(step_launches + decode_launches) * steps, partial=partial_kernel_name(case.cfg))
+             eager_ms=sum(eager_ms) / len(eager_ms), launches=(step_launches + 2 * decode_launches) * steps,
+             partial=partial_kernel_name(case.cfg))
     if "mma" in r["partial"] and not e2e_steps:
         r["fixed_shift"] = time_fixed_shift(sess, steps, flush, sink, stream)
     if e2e_steps:
@@ -513,6 +529,7 @@ def run_gpu(args, rank: int, world: int):
     kv_bytes = case.kv_bytes()
     out = dict(case=case, kv_bytes=kv_bytes, total_bytes=all_reduce_sum(float(kv_bytes), world),
                ms_per_step=all_reduce_max(r["ms_per_step"], world), dec_ms=all_reduce_max(r["dec_ms"], world),
+               eager_ms=all_reduce_max(r["eager_ms"], world),
                e2e_ms=all_reduce_max(r["e2e_ms"], world), h2d=r["h2d"], d2h=r["d2h"], clocks=clocks.summary(),
                launches=r["launches"], step_ms=r["step_ms"], partial=r["partial"])
     # every other workload, timed the same way (one GPU only: they are not replicas)
@@ -529,7 +546,8 @@ def run_gpu(args, rank: int, world: int):
             roof = roofline(c, rr["dec_ms"], peaks)
             per[name] = {"partial_kernel": rr["partial"], "steps": steps, "us_per_step": round(rr["ms_per_step"] * 1e3, 3),
                          "step_kv_gbs": round(c.kv_bytes() / (rr["ms_per_step"] * 1e-3) / 1e9, 2),
-                         "decode_us": round(rr["dec_ms"] * 1e3, 3), "kv_bytes": int(c.kv_bytes()),
+                         "decode_us": round(rr["dec_ms"] * 1e3, 3),
+                         "decode_eager_us": round(rr["eager_ms"] * 1e3, 3), "kv_bytes": int(c.kv_bytes()),
                          "roofline": {**roof, "traffic": profiled_traffic(name, c.kv_bytes())},
                          "clocks": clk.summary()}
             if "fixed_shift" in rr:
@@ -594,7 +612,9 @@ def config_block(case, args, arm: str = "gpu"):
             else "n/a (CPU)",
             "step": "append of the step's new positions + split plan + split-KV partial + fixed-order merge"
             if arm == "gpu" else "the oracle's append of the new positions + float64 attention, bounded sample",
-            "timing": "CUDA events per step around a CUDA-graph replay of the step" if arm == "gpu"
+            "timing": "CUDA events per step around a CUDA-graph replay of the step; the roofline's decode call "
+                      "(plan + partial + merge) likewise around a graph replay of the call alone, with the eagerly "
+                      "launched call's time beside it (us_per_launch_eager)" if arm == "gpu"
             else "wall clock (time.perf_counter) around each sample"}
 
 
@@ -665,7 +685,8 @@ def main():
         "data": "synthetic (seeded: workloads/)",
         "config": config_block(case, args),
         "roofline": {"kernel": f"decode call (plan_kernel + {r['partial']} + decode_merge_kernel)", **roof,
-                     "us_per_launch": round(r["dec_ms"] * 1e3, 3), "traffic": traffic,
+                     "us_per_launch": round(r["dec_ms"] * 1e3, 3),
+                     "us_per_launch_eager": round(r["eager_ms"] * 1e3, 3), "traffic": traffic,
                      "algorithmic_bytes_per_launch": int(r["kv_bytes"])},
         "per_config": r["per_config"],
         "cpu_baseline": {"value": round(cpu_bytes / cpu_s / 1e9, 4) if cpu_s > 0 else None, "unit": "GB/s",

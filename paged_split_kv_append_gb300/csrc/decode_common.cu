@@ -9,6 +9,14 @@ namespace nbx {
 constexpr int kPlanThreads = 256;
 constexpr int kSortMax = 2048;   // batches up to this size are planned in shared memory, longest split first
 
+// Dynamic shared memory of the plan kernel: five int arrays of the batch (4 (5B + 1) bytes), none
+// above kSortMax. Sized to the batch, so that the CTA leaves room on its SM for a CTA of the
+// partial kernel that follows it (launched while the plan runs): a fixed 40 KB took that room from
+// one tensor-core CTA, whose late start lengthened a one-wave grid by the plan's own time.
+inline size_t plan_smem_bytes(int batch) {
+  return batch <= kSortMax ? static_cast<size_t>(5 * batch + 1) * sizeof(int) : 0;
+}
+
 // Positions per split of the SIMT partial kernel: two of the pages' splits (NBX_SPLIT_POSITIONS).
 // Each work unit of the persistent kernel pays about 2.4 us at its boundaries (the cross-warp merge
 // and the partial's stores, the next unit's query staging and first stage); at 512 positions a unit
@@ -65,11 +73,12 @@ __device__ __forceinline__ void plan_finish(const DecodeParams& p) {
 // otherwise the pages' rule. Two instantiations keep the pages' rule's code free of the other.
 template <bool TC>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
-  __shared__ int s_len[kSortMax];
-  __shared__ int s_seg[kSortMax];
-  __shared__ int s_n[kSortMax];
-  __shared__ int s_order[kSortMax];
-  __shared__ int s_base[kSortMax + 1];
+  extern __shared__ int plan_sm[];   // plan_smem_bytes(batch)
+  int* const s_len = plan_sm;
+  int* const s_seg = s_len + p.batch;
+  int* const s_n = s_seg + p.batch;
+  int* const s_order = s_n + p.batch;
+  int* const s_base = s_order + p.batch;   // [batch + 1]
   __shared__ int s_warp[kPlanThreads / 32];
   __shared__ int s_empty;
   __shared__ int s_nb;
@@ -515,8 +524,9 @@ cudaError_t decode_dispatch(const DecodeParams& p, int q_dtype, int pool_dtype, 
     q.tc_units = device_info().sm_count;
     q.tc_pairs = p.h_kv * ((p.rows * p.group + kMmaRowsPerTile - 1) / kMmaRowsPerTile);
   }
-  cudaError_t e = q.tc_units > 0 ? launch_pdl(plan_kernel<true>, 1u, kPlanThreads, 0, stream, q)
-                                 : launch_pdl(plan_kernel<false>, 1u, kPlanThreads, 0, stream, q);
+  const size_t plan_smem = plan_smem_bytes(q.batch);
+  cudaError_t e = q.tc_units > 0 ? launch_pdl(plan_kernel<true>, 1u, kPlanThreads, plan_smem, stream, q)
+                                 : launch_pdl(plan_kernel<false>, 1u, kPlanThreads, plan_smem, stream, q);
   if (e != cudaSuccess) return e;
   if (mma) e = decode_dispatch_mma(q, pool_dtype, grid_limit, stream);
   else if (pool_dtype == NBX_F32) e = decode_dispatch_F32(q, q_dtype, grid_limit, stream);

@@ -180,8 +180,8 @@ def test_fp8_attention_sink_with_heavy_tail():
 
 def test_fp8_flat_tail_far_below_a_sink():
     # Every query vector is e_0 and key j is t_j e_0, so a score is t_j * scale exactly (the sink's
-    # key is the pool's largest, code 448): a sink 14.415 log2 units above 5,999 zero-score keys.
-    # With m 6 below the sink each tail weight is 2^-8.415 = 1.498 * 2^-9, which the E4M3 terms
+    # key is the pool's largest, code 448): a sink 13.415 log2 units above 5,999 zero-score keys.
+    # With m 5 below the sink each tail weight is 2^-8.415 = 1.498 * 2^-9, which the E4M3 terms
     # round to 2^-8 (+33 %), the same way for every key. The tail holds a fifth of the weight and
     # its values are all +3 (the sink's -3). A window of 128 rows over 6,000 keys is cut into
     # splits of 1,024: an output that kept the sink split's tail weights would be off by ~0.1.
@@ -191,7 +191,7 @@ def test_fp8_flat_tail_far_below_a_sink():
     case = wl.make_case(cfg, device=DEV)
     case.q.zero_()
     case.q[..., 0] = 1.0
-    b_sink = 14.415 / (case.scale * np.log2(np.e))
+    b_sink = 13.415 / (case.scale * np.log2(np.e))
     case.k_raw.zero_()
     case.v_raw.fill_(3.0)
     for b in range(cfg.batch):
