@@ -327,12 +327,12 @@ NBX_API void nbx_set_decode_grid_limit(int max_ctas);
 
 /*
  * nbx_set_decode_wait_test -- for tests of the timeout path only; the pages have no counterpart.
- * Every wait inside the SIMT split-partial kernel is bounded (2 s by default): a wait that runs out
- * sets NBX_DEV_TIMEOUT, the kernel lets its copies in flight land and returns, and the output of the
- * call is incomplete. This sets that bound (wait_limit_ns; 0 restores 2 s) and holds each CTA's
- * producer warp back for producer_delay_ns before it starts (0 = no delay; capped at 50 ms), so a
- * test can make the consumers' waits run out without any invalid input. Process-wide; applies to
- * calls launched after it; the tensor-core kernels keep their own 2 s bound.
+ * Every wait inside the split-partial kernels is bounded (2 s by default): a wait that runs out
+ * sets NBX_DEV_TIMEOUT, the kernel lets its copies in flight land (and, on tensor cores, its MMAs
+ * complete and its TMEM go back) and returns, and the output of the call is incomplete. This sets
+ * that bound (wait_limit_ns; 0 restores 2 s) and holds each CTA's producer warps back for
+ * producer_delay_ns before they start (0 = no delay; capped at 50 ms), so a test can make the other
+ * warps' waits run out without any invalid input. Process-wide; applies to calls launched after it.
  */
 NBX_API void nbx_set_decode_wait_test(unsigned long long wait_limit_ns, unsigned long long producer_delay_ns);
 

@@ -116,20 +116,21 @@ struct MmaMaps {
 };
 
 // Bounded wait that also gives up when another role of the CTA has given up.
-__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// limit_ns: DecodeParams::wait_limit_ns (2 s unless a test of the timeout path shortens it).
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((i & 3u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 3u) == 0u && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
 // The same, with one answer for the whole warp (the tcgen05 .sync.aligned forms that follow need
 // every lane).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  return __all_sync(0xffffffffu, bwait(bar, parity, abort_flag));
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, bwait(bar, parity, abort_flag, limit_ns));
 }
 
 struct MmaUnit {
@@ -406,6 +407,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint64_t wlim = p.wait_limit_ns;
   pdl_wait();   // the plan kernel's work list and the append's positions are visible from here on
   pdl_launch_dependents();
 
@@ -424,6 +426,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     uint64_t* rfull = is_k ? kfull : vfull;
     uint64_t* rempty = is_k ? kempty : vempty;
     const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+    if (p.producer_delay_ns) {   // a test holds the producers back so that the other roles' waits run out
+      const uint64_t t0 = global_timer_ns();
+      while (global_timer_ns() - t0 < p.producer_delay_ns) __nanosleep(10000);
+    }
     bool ok = true;
     uint32_t i = 0;   // ring ordinal
     TileIter it;
@@ -435,7 +441,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int row0 = tile_row(p, it.mu, it.mu.start + t * kMmaN, ps.page(t), lane == 0 && is_k);
       for (int j = 0; j < HI; ++j, ++i) {
         int r = 1;
-        if (lane == 0 && i >= static_cast<uint32_t>(NR)) r = bwait(&rempty[i % NR], (i / NR - 1) & 1u, abort_flag);
+        if (lane == 0 && i >= static_cast<uint32_t>(NR)) r = bwait(&rempty[i % NR], (i / NR - 1) & 1u, abort_flag, wlim);
         if (!__shfl_sync(0xffffffffu, r, 0)) {
           ok = false;
           break;
@@ -479,9 +485,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       while (!it.done) {
         // S(x) = Q K(x)^T once the buffer's previous PV is done, K(x) has landed and the unit's Q has
         const uint32_t ki = it.item(it.t);
-        if (it.x >= static_cast<uint32_t>(kSBufs)) ok = bwait(&sp_free[sx], (sxp - 1) & 1u, abort_flag);
-        for (int j = 0; j < HI && ok; ++j) ok = bwait(&kfull[(ki + j) % NK], ((ki + j) / NK) & 1u, abort_flag);
-        if (ok && it.t == 0) ok = bwait(q_full, it.k & 1u, abort_flag);
+        if (it.x >= static_cast<uint32_t>(kSBufs)) ok = bwait(&sp_free[sx], (sxp - 1) & 1u, abort_flag, wlim);
+        for (int j = 0; j < HI && ok; ++j) ok = bwait(&kfull[(ki + j) % NK], ((ki + j) / NK) & 1u, abort_flag, wlim);
+        if (ok && it.t == 0) ok = bwait(q_full, it.k & 1u, abort_flag, wlim);
         if (!ok) break;
         tc_fence_after();
         if (it.t == 0) fence_proxy_async();   // Q was written by cp.async or st.shared (generic proxy)
@@ -534,7 +540,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       bool ok = true;
       for (uint32_t k = 0; !it.done; ++k) {
         int r = 1;
-        if (lane == 1 && k > 0) r = bwait(q_empty, (k - 1) & 1u, abort_flag);
+        if (lane == 1 && k > 0) r = bwait(q_empty, (k - 1) & 1u, abort_flag, wlim);
         if (!__shfl_sync(kLoaders, r, 1)) {
           ok = false;
           break;
@@ -595,9 +601,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       while (!it.done) {
         // O += P(y) V(y): P written, V landed, O read out by the previous unit's epilogue
         const uint32_t vi = it.item(it.t);
-        ok = bwait(&p_full[sy], syp & 1u, abort_flag);
-        if (ok && it.t == 0 && it.k > 0) ok = bwait(o_free, (it.k - 1) & 1u, abort_flag);
-        for (int j = 0; j < HI && ok; ++j) ok = bwait(&vfull[(vi + j) % NV], ((vi + j) / NV) & 1u, abort_flag);
+        ok = bwait(&p_full[sy], syp & 1u, abort_flag, wlim);
+        if (ok && it.t == 0 && it.k > 0) ok = bwait(o_free, (it.k - 1) & 1u, abort_flag, wlim);
+        for (int j = 0; j < HI && ok; ++j) ok = bwait(&vfull[(vi + j) % NV], ((vi + j) / NV) & 1u, abort_flag, wlim);
         if (!ok) break;
         const int valid = min(kMmaN, it.mu.end - (it.mu.start + it.t * kMmaN));
         const int ksteps = (valid + kStep - 1) / kStep;
@@ -698,7 +704,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if ((t & 31) == 31) pg_cur = pg_nxt;
         const bool tile_ok = page >= 0 && page < p.num_pages;
         const uint32_t sbuf = tmem + gb * kMmaN;
-        if (!warp_wait(&s_full[gb], gp & 1u, abort_flag)) {
+        if (!warp_wait(&s_full[gb], gp & 1u, abort_flag, wlim)) {
           ok = false;
           break;
         }
@@ -817,7 +823,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         if (t > 0 && __any_sync(0xffffffffu, f != 1.f)) {
           // O holds the PVs of tiles g-t .. g-1: wait for the last, then rescale it in TMEM, 64
           // columns a round with the loads in flight together
-          if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
+          if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag, wlim)) {
             ok = false;
             break;
           }
@@ -860,7 +866,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         }
       }
       // ---- the unit's last PV is done: O is complete
-      if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag)) {
+      if (!warp_wait(&sp_free[pb], pp & 1u, abort_flag, wlim)) {
         ok = false;
         break;
       }

@@ -127,9 +127,9 @@ def test_one_cta_runs_every_unit(d, h_q, h_kv, page):
     check_against_oracle(case, sess, out)
 
 
-def fp8_config(name, lens, seed, rows=16, page=64):
-    cfg = wl.Config(name, len(lens), rows, 24, 4, 256, page, "e4m3", "bf16", seed, ("fixed", tuple(lens)))
-    kind = nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, rows, 24, 4, 256, 1000, page)
+def fp8_config(name, lens, seed, rows=16, page=64, h_q=24, h_kv=4, d=256):
+    cfg = wl.Config(name, len(lens), rows, h_q, h_kv, d, page, "e4m3", "bf16", seed, ("fixed", tuple(lens)))
+    kind = nbx.nbx_paged_decode_partial_kernel(nbx.NBX_BF16, nbx.NBX_E4M3, rows, h_q, h_kv, d, 1000, page)
     assert kind == nbx.PARTIAL_TCGEN05_FP8
     return cfg
 
@@ -139,6 +139,41 @@ def test_fp8_pool_window_on_the_codes():
     cfg = fp8_config("tc_fp8", (1, 64, 100, 700, 1500), 36)
     case = wl.make_case(cfg, device=DEV)
     sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+
+
+@pytest.mark.parametrize("rows,h_q,h_kv,page", [(16, 32, 4, 128), (8, 64, 2, 64)])
+def test_fp8_window_head_dim_128(rows, h_q, h_kv, page):
+    # d = 128: one 128-code atom per K and V tile row (the d = 256 windows have two); a group of 8
+    # (one full M tile of 16 rows) on 128-position pages, and a group of 32 (two tiles of 4 rows)
+    cfg = fp8_config(f"tc_fp8_d128_{h_q}", (1, 63, 64, 65, 700, 2500), 44, rows=rows, page=page, h_q=h_q,
+                     h_kv=h_kv, d=128)
+    case = wl.make_case(cfg, device=DEV)
+    sess, out = run_step(case)
+    check_against_oracle(case, sess, out)
+    _, o2 = run_step(case, grid_limit=3)
+    assert torch.equal(o2, out)
+
+
+@pytest.mark.parametrize("name", ["verify_small", "prefill_small"])
+def test_a_tensor_core_wait_that_runs_out_sets_the_timeout_bit_and_returns(name):
+    # The producer warps are held back 20 ms and every wait is bounded at 20 us: the MMA issuers'
+    # and the softmax warps' waits run out, the kernel records NBX_DEV_TIMEOUT, lets the copies the
+    # producers then issue land, waits for its MMAs, releases its TMEM and returns. The call
+    # completes and the next call is correct (bf16 and fp8 pools).
+    case = wl.make_case(name, device=DEV)
+    sess = bench.session_for_case(case, DEV)
+    torch.cuda.synchronize()
+    try:
+        nbx.nbx_set_decode_wait_test(20_000, 20_000_000)
+        sess.step()
+        torch.cuda.synchronize()
+    finally:
+        nbx.nbx_set_decode_wait_test(0, 0)
+    assert sess.status_bits() & nbx.DEV_TIMEOUT
+    sess.status.zero_()
+    out = sess.decode().clone()
+    torch.cuda.synchronize()
     check_against_oracle(case, sess, out)
 
 
