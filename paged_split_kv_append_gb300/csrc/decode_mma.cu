@@ -116,7 +116,9 @@ struct MmaMaps {
 };
 
 // Bounded wait that also gives up when another role of the CTA has given up.
-// limit_ns: DecodeParams::wait_limit_ns (2 s unless a test of the timeout path shortens it).
+// limit_ns: kWaitLimitNs (2 s), or DecodeParams::wait_limit_ns in the instantiation a test of the
+// timeout path runs (a bound read at run time cost the fp8 window 8 us a call, so the kernels of
+// normal calls keep the constant).
 __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -129,7 +131,8 @@ __device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile i
 
 // The same, with one answer for the whole warp (the tcgen05 .sync.aligned forms that follow need
 // every lane).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
   return __all_sync(0xffffffffu, bwait(bar, parity, abort_flag, limit_ns));
 }
 
@@ -335,8 +338,10 @@ __device__ __forceinline__ float q_to_e4m3_terms(const DecodeParams& p, const Mm
 }
 
 // F8: the pools hold E4M3 codes, read as they are by kind::f8f6f4 MMAs (Q and P as two E4M3 terms
-// each); otherwise bf16 pools and kind::f16 MMAs (P as two bf16 terms).
-template <int D, bool F8>
+// each); otherwise bf16 pools and kind::f16 MMAs (P as two bf16 terms). TW: a test of the timeout
+// path (nbx_set_decode_wait_test): the waits take DecodeParams::wait_limit_ns and the producers
+// start after DecodeParams::producer_delay_ns.
+template <int D, bool F8, bool TW>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     decode_partial_mma_kernel(DecodeParams p, const __grid_constant__ MmaMaps maps) {
   using C = MmaCfg<D, F8>;
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint64_t wlim = p.wait_limit_ns;
+  const uint64_t wlim = TW ? p.wait_limit_ns : kWaitLimitNs;
   pdl_wait();   // the plan kernel's work list and the append's positions are visible from here on
   pdl_launch_dependents();
 
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     uint64_t* rfull = is_k ? kfull : vfull;
     uint64_t* rempty = is_k ? kempty : vempty;
     const CUtensorMap* map = is_k ? &maps.k : &maps.v;
-    if (p.producer_delay_ns) {   // a test holds the producers back so that the other roles' waits run out
+    if (TW && p.producer_delay_ns) {   // a test holds the producers back so that the other roles' waits run out
       const uint64_t t0 = global_timer_ns();
       while (global_timer_ns() - t0 < p.producer_delay_ns) __nanosleep(10000);
     }
@@ -1026,9 +1031,11 @@ cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t strea
   if (maps == nullptr) return cudaErrorInvalidValue;
   const uint64_t bit = 1ull << (di.device & 63);
   if ((configured.load() & bit) == 0) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(decode_partial_mma_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(decode_partial_mma_kernel<D, F8, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_partial_mma_kernel<D, F8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::kSmem);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
@@ -1038,7 +1045,10 @@ cudaError_t launch_mma(const DecodeParams& p, int grid_limit, cudaStream_t strea
   if (grid_limit > 0 && grid > grid_limit) grid = grid_limit;
   if (grid > upper) grid = upper;
   if (grid < 1) grid = 1;
-  return launch_pdl(decode_partial_mma_kernel<D, F8>, static_cast<unsigned>(grid), kMmaThreads, C::kSmem,
+  if (p.wait_limit_ns != kWaitLimitNs || p.producer_delay_ns != 0)   // a test of the timeout path
+    return launch_pdl(decode_partial_mma_kernel<D, F8, true>, static_cast<unsigned>(grid), kMmaThreads, C::kSmem,
+                      stream, p, *maps);
+  return launch_pdl(decode_partial_mma_kernel<D, F8, false>, static_cast<unsigned>(grid), kMmaThreads, C::kSmem,
                     stream, p, *maps);
 }
 
