@@ -62,7 +62,7 @@ def test_noalloc_decode_matches_the_workspace_decode_twice(name, kernel):
     ref = sess.step().clone()                  # the existing entry point, with its own workspace
     torch.cuda.synchronize()
     assert sess.status_bits() == 0
-    # the fixed scratch holds what this call needs, including the bf16 copies of an fp8 window
+    # the fixed scratch holds what this call needs
     need = nbx.nbx_paged_decode_workspace_bytes_for(nbx.dtype_code(case.q), nbx.dtype_code(sess.k_pool), cfg.batch,
                                                     cfg.rows, cfg.h_q, cfg.h_kv, cfg.d, case.max_seq_len,
                                                     cfg.page_tokens)
