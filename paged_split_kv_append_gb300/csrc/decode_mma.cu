@@ -41,16 +41,17 @@
 //    is exact and the others are off by at most 2^-16 of it; the softmax threads write them (one
 //    query vector each) and fold 2^-e into their row's scale. P enters as P_hi + P_lo, the same
 //    split of p: each p is off by at most 2^-9 p, plus 2^-9 when p < 2^-1 (E4M3 holds nothing
-//    below 2^-9). The running max m moves up when a tile's max passes m + 8.75 (p stays below
-//    448) and down when a tile holds more weights below 2^-1 than its largest weight, so each
-//    tile's weights are off by at most 2^-8 of their sum.
-//    O and l are rescaled in TMEM whenever m moves, downwards only while the weight gathered stays
-//    below 2^40 (past that the tile, below 2^15, adds less than 2^-25 of the total).
+//    below 2^-9). The running max m moves up, to 5 below a tile's max, when that passes m + 8.75
+//    (p stays below 448). A budget keeps the absolute parts within 2^-8 of the weight gathered:
+//    a tile that could pass it has its small weights counted, and if they do pass it, m moves
+//    down to 5 below the tile's max -- only while the weight gathered stays below 2^40 (past that
+//    the tile, below 2^15, adds less than 2^-25 of the total). O and l are rescaled in TMEM
+//    whenever m moves.
 //  * warps 0-3 (softmax, one query vector per thread = one TMEM lane): read S from TMEM, mask
 //    (split end, causal row position, missing pages), run the online softmax in log2 units with
 //    the lazy rescale (O is rescaled in TMEM only when a row's max grows by more than 2^8; with an
-//    fp8 pool, also when it falls, as above), and write P_hi / P_lo over the S columns they came
-//    from. After the unit's last PV each thread
+//    fp8 pool as above), and write P_hi / P_lo over the S columns they came from, then, when m
+//    moved, wait for the last PV into O and rescale it. After the unit's last PV each thread
 //    stores its own row of O, 32 columns at a time, from registers with 32-byte stores -- the
 //    partial, or the normalised output when the sequence has one split.
 //  * Every wait is bounded. On timeout the kernel records NBX_DEV_TIMEOUT, waits (bounded) for
