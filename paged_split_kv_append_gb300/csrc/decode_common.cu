@@ -67,10 +67,11 @@ __device__ __forceinline__ void plan_finish(const DecodeParams& p) {
 
 // Reads the device lengths, writes every sequence's plan (len, positions per split, non-empty
 // splits), zeroes the work counter, writes 0 to the output rows of empty sequences, and writes
-// the work list of (sequence, split) entries: sequences with the longest splits first (stable),
-// splits ascending. Batches above kSortMax keep their own order and take a slower serial path.
+// the work list of (sequence, split) entries: every sequence's last split first, then the other
+// splits, sequences with the longest splits first (stable), splits ascending. Batches above kSortMax
+// keep their own order and take a slower serial path.
 // TC: a tensor-core window, whose splits are sized by the call's total work (DecodeParams::tc_units);
-// otherwise the pages' rule. Two instantiations keep the pages' rule's code free of the other.
+// otherwise splits of kSimtSplitPositions. Two instantiations keep each rule's code free of the other.
 template <bool TC>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(DecodeParams p) {
   extern __shared__ int plan_sm[];   // plan_smem_bytes(batch)
